@@ -1,0 +1,173 @@
+"""Float64 CPU oracle for branch-replay attention.  TEST INFRASTRUCTURE ONLY.
+
+Only the tests, the smoke check and the benchmark's CPU-baseline leg may import this
+module.  It shares no code with the CUDA path.
+
+What it computes (LongStraw review, dimensionstp.github.io "LongStraw", sections 2-1 and
+3-2 (4): the prompt is captured once without autograd and each response is replayed on
+its own against it, forward and backward, and the gradients are summed over the group):
+
+  for one response i, build the concatenated sequence X_i = [prompt; response_i] of
+  length N = P + R_i and run ordinary causal softmax attention for the response rows.
+  Suffix row t (0-based) sees every prompt key and the response keys 0..t, i.e. the
+  keys j <= P + t of X_i.
+
+  S = s * Q K^T (s = 1/sqrt(D) unless given), P = softmax_row(S), O = P V,
+  LSE = log sum_j exp(S_j)  (natural log).
+
+  The backward is written out by the explicit formulas of softmax attention, with the
+  upstream gradient dO given on the response rows and zero on the prompt rows (the
+  prompt rows carry no loss: the prompt is captured without a graph):
+    dV = P^T dO,  dP = dO V^T,  dS = P * (dP - rowsum(P * dP)),
+    dQ = s dS K,  dK = s dS^T Q.
+  Grouped-query attention: query head h reads kv head floor(h / g), g = Hq / Hkv, and the
+  kv-head gradients sum over the g query heads of the group.
+
+  The gradient w.r.t. the prompt keys/values, summed over the G responses of a group, is
+  the quantity the prompt-side term of the gradient decomposition (review section 2-2,
+  the equation splitting the total gradient at the prompt boundary state z_P) needs for
+  this layer.
+
+Pins (tests/test_oracle_attention.py): central finite differences of <O, dO>, torch fp64
+autograd on one packed prompt+all-responses sequence with a block mask (the shared
+prefix tree), scaled_dot_product_attention in fp64, closed forms (equal keys -> mean of
+the visible values, constant values -> that value), shift invariance of the keys and the
+sum rules over keys.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = ["replay_response", "replay_group", "response_rows"]
+
+_ROW_CHUNK = 256
+
+
+def _f64(x):
+    """Exact upcast of a bf16/fp32 torch tensor or array to a float64 numpy array."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            return x.detach().to("cpu", torch.float64).numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.asarray(x, dtype=np.float64)
+
+
+def _kv_of(h: int, Hq: int, Hkv: int) -> int:
+    return h // (Hq // Hkv)
+
+
+def replay_response(k_prefix, v_prefix, q, k_suffix, v_suffix, d_out, scale=None,
+                    heads=None, want_grads=True):
+    """Forward and backward of one response replayed against the prompt.
+
+    Shapes: k_prefix, v_prefix [P, Hkv, D]; q, d_out [R, Hq, D]; k_suffix, v_suffix
+    [R, Hkv, D].  `heads` restricts the work to a subset of query heads (the kv-head
+    gradients then contain only those heads' contributions).
+
+    Returns a dict of float64 arrays: o [R,Hq,D], lse [R,Hq], and with want_grads
+    dq [R,Hq,D], dk_prefix/dv_prefix [P,Hkv,D], dk_suffix/dv_suffix [R,Hkv,D].
+    Entries for query heads outside `heads` stay zero.
+    """
+    Kp, Vp, Q, Ks, Vs = (_f64(a) for a in (k_prefix, v_prefix, q, k_suffix, v_suffix))
+    dO = _f64(d_out) if want_grads else None
+    P, Hkv, D = Kp.shape
+    R, Hq, _ = Q.shape
+    s = (1.0 / np.sqrt(D)) if scale is None else float(scale)
+    heads = range(Hq) if heads is None else heads
+    N = P + R
+
+    o = np.zeros((R, Hq, D))
+    lse = np.zeros((R, Hq))
+    if want_grads:
+        dq = np.zeros((R, Hq, D))
+        dk = np.zeros((N, Hkv, D))
+        dv = np.zeros((N, Hkv, D))
+
+    for h in heads:
+        kv = _kv_of(h, Hq, Hkv)
+        K = np.concatenate([Kp[:, kv, :], Ks[:, kv, :]], axis=0)   # keys of X_i
+        Vv = np.concatenate([Vp[:, kv, :], Vs[:, kv, :]], axis=0)
+        for t0 in range(0, R, _ROW_CHUNK):
+            t1 = min(R, t0 + _ROW_CHUNK)
+            t = np.arange(t0, t1)
+            S = s * (Q[t0:t1, h, :] @ K.T)                           # [c, N]
+            visible = np.arange(N)[None, :] <= (P + t)[:, None]
+            S = np.where(visible, S, -np.inf)
+            m = S.max(axis=1, keepdims=True)
+            E = np.exp(S - m)
+            l = E.sum(axis=1, keepdims=True)
+            Pm = E / l
+            lse[t0:t1, h] = (m + np.log(l))[:, 0]
+            o[t0:t1, h, :] = Pm @ Vv
+            if want_grads:
+                g = dO[t0:t1, h, :]
+                dP = g @ Vv.T
+                dS = Pm * (dP - (Pm * dP).sum(axis=1, keepdims=True))
+                dq[t0:t1, h, :] = s * (dS @ K)
+                dk[:, kv, :] += s * (dS.T @ Q[t0:t1, h, :])
+                dv[:, kv, :] += Pm.T @ g
+
+    out = {"o": o, "lse": lse}
+    if want_grads:
+        out.update(dq=dq, dk_prefix=dk[:P], dv_prefix=dv[:P],
+                   dk_suffix=dk[P:], dv_suffix=dv[P:])
+    return out
+
+
+def replay_group(k_prefix, v_prefix, responses, scale=None, heads=None):
+    """Serial replay of every response of a group; prompt gradients summed over the group.
+
+    `responses` is a sequence of (q, k_suffix, v_suffix, d_out) tuples.  Returns
+    (per_response_results, dk_prefix_sum, dv_prefix_sum).
+    """
+    Kp, Vp = _f64(k_prefix), _f64(v_prefix)
+    dk_sum = np.zeros(Kp.shape)
+    dv_sum = np.zeros(Vp.shape)
+    results = []
+    for (q, ks, vs, do) in responses:
+        r = replay_response(Kp, Vp, q, ks, vs, do, scale=scale, heads=heads)
+        dk_sum += r["dk_prefix"]
+        dv_sum += r["dv_prefix"]
+        results.append(r)
+    return results, dk_sum, dv_sum
+
+
+def response_rows(k_prefix, v_prefix, q, k_suffix, v_suffix, d_out, rows, scale=None):
+    """O, LSE and dQ of selected (t, h) query rows of one response, each row exact.
+
+    The outputs of one row depend only on that row's query, its upstream gradient and
+    the keys/values it sees, so a row can be checked on its own at any prompt length.
+    Returns (o [n,D], lse [n], dq [n,D]) in the order of `rows`.
+    """
+    Q = _f64(q)
+    dO = _f64(d_out)
+    P, Hkv, D = k_prefix.shape
+    R, Hq, _ = Q.shape
+    s = (1.0 / np.sqrt(D)) if scale is None else float(scale)
+    n = len(rows)
+    o = np.zeros((n, D))
+    lse = np.zeros(n)
+    dq = np.zeros((n, D))
+    by_kv = {}
+    for idx, (t, h) in enumerate(rows):
+        by_kv.setdefault(_kv_of(h, Hq, Hkv), []).append(idx)
+    for kv, idxs in by_kv.items():
+        K = np.concatenate([_f64(k_prefix[:, kv, :]), _f64(k_suffix[:, kv, :])], axis=0)
+        Vv = np.concatenate([_f64(v_prefix[:, kv, :]), _f64(v_suffix[:, kv, :])], axis=0)
+        for idx in idxs:
+            t, h = rows[idx]
+            Kt = K[:P + t + 1]                        # keys visible from suffix row t
+            Vt = Vv[:P + t + 1]
+            S = s * (Kt @ Q[t, h, :])
+            m = S.max()
+            E = np.exp(S - m)
+            l = E.sum()
+            Pm = E / l
+            lse[idx] = m + np.log(l)
+            o[idx] = Pm @ Vt
+            dP = Vt @ dO[t, h, :]
+            dS = Pm * (dP - (Pm * dP).sum())
+            dq[idx] = s * (dS @ Kt)
+    return o, lse, dq
