@@ -1,0 +1,198 @@
+/*
+ * longstraw.h -- C ABI of the GB300 branch-replay library.
+ *
+ * The library implements the per-GPU hot path of LongStraw-style branch replay for GRPO
+ * (LongStraw review, dimensionstp.github.io "LongStraw": section 1-1 problem definition and
+ * the L_policy equation; section 2-1 the five-step transaction; section 3-2 (1) no-grad
+ * prompt capture, (3) restore without mutating the prompt state, (4) serial suffix replay;
+ * section 4-3 (5) the architecture-adapter interface).  One call sequence per GRPO group:
+ *
+ *   ls_prefix_prepare          register the resident prompt K/V, zero the fp32 accumulators
+ *   for each response i (serially, on one stream):
+ *     ls_replay_fwd            suffix attention over [prompt; response_i], causal suffix
+ *     ls_grpo_loss             clipped-surrogate loss contribution + dlogits
+ *     ls_replay_bwd            dQ, suffix dK/dV; prompt dK/dV added into the accumulators
+ *   ls_prefix_grad_finalize    one finalization of the group-summed prompt gradient
+ *
+ * Conventions shared by every entry point
+ *  - Pointers named "device" must point to device memory of the current CUDA device,
+ *    allocated and owned by the caller.  The library allocates no device memory and never
+ *    frees caller memory; it keeps only host-side metadata in the prefix handle.
+ *  - Tensors are dense row-major.  "THD" means [tokens, heads, head_dim], contiguous.
+ *    bf16 is IEEE bfloat16 stored in 2 bytes.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  All
+ *    work is enqueued on it; calls return before the GPU finishes.
+ *  - Argument errors are detected on the host and returned before anything is enqueued.
+ *    Launch failures return LS_ERR_CUDA; ls_last_error() gives the CUDA message.
+ *    Kernels never trap: a device-side check that fails (a bounded wait that gave up, an
+ *    index outside its buffer) sets a device status word that ls_get_device_status()
+ *    reads back.
+ *  - Prompt-gradient accumulation is atomic-free: every ls_replay_bwd on one handle must
+ *    be ordered on one stream (or otherwise serialised by the caller).  The handle is not
+ *    thread-safe.
+ */
+#ifndef LONGSTRAW_H
+#define LONGSTRAW_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LS_OK = 0,
+  LS_ERR_INVALID_ARGUMENT = 1, /* null pointer, non-positive size, bad enum value        */
+  LS_ERR_UNSUPPORTED = 2,      /* shape outside the supported set (see ls_prefix_desc)  */
+  LS_ERR_NOT_PREPARED = 3,     /* handle is NULL, destroyed or not from ls_prefix_prepare */
+  LS_ERR_MISALIGNED = 4,       /* a device pointer is not 16-byte aligned               */
+  LS_ERR_CUDA = 5,             /* a CUDA runtime/driver call or a launch failed         */
+  LS_ERR_TIMEOUT = 6,          /* a kernel's bounded wait gave up (device status)       */
+  LS_ERR_DEVICE_STATUS = 7,    /* a kernel recorded another device-side check failure   */
+  LS_ERR_WORKSPACE = 8,        /* workspace pointer NULL or smaller than required       */
+  LS_ERR_WRONG_DEVICE = 9      /* current device or stream device differs from handle's */
+} ls_status;
+
+/* Opaque prefix handle: host metadata and TMA descriptors of the resident prompt K/V. */
+typedef struct ls_prefix_s* ls_prefix_t;
+
+/*
+ * Description of the resident prompt state of ONE attention layer (the captured
+ * "continuation state" of the review's section 3-2 (1): the prompt's keys and values).
+ *   P              prompt length, 1 <= P < 2^31.
+ *   Hq, Hkv        query and key/value heads; Hq % Hkv == 0 and g = Hq/Hkv <= 16.  Query
+ *                  head h reads kv head h / g (contiguous groups).
+ *   D              head dimension, 64 or 128.
+ *   softmax_scale  scale s applied to q.k; 0 selects 1/sqrt(D).
+ *   k_prefix, v_prefix  device, bf16 THD [P, Hkv, D], 16-byte aligned.  Borrowed: they
+ *                  must stay valid and unmodified until ls_prefix_destroy; the library
+ *                  only reads them (the review's rule that a replay must not mutate the
+ *                  shared prompt state, section 3-2 (3)).
+ *   dk_acc, dv_acc device, fp32 [P, Hkv, D], 16-byte aligned.  Borrowed; zeroed by
+ *                  ls_prefix_prepare, then each ls_replay_bwd adds that response's
+ *                  d loss / d (prompt K, V) into them.
+ */
+typedef struct {
+  int64_t P;
+  int32_t Hq;
+  int32_t Hkv;
+  int32_t D;
+  float softmax_scale;
+  const void* k_prefix;
+  const void* v_prefix;
+  float* dk_acc;
+  float* dv_acc;
+} ls_prefix_desc;
+
+/*
+ * ls_prefix_prepare -- prompt capture hand-off (review section 2-1 step 1; section 3-2 (1)).
+ * Validates `desc`, encodes the TMA descriptors of the prompt K/V once, and enqueues the
+ * zeroing of dk_acc/dv_acc on `stream`.  On success *out receives a new handle bound to
+ * the current device.  On error *out is left unchanged and nothing is enqueued.
+ */
+ls_status ls_prefix_prepare(const ls_prefix_desc* desc, ls_prefix_t* out, void* stream);
+
+/* Release the handle's host metadata.  Does not touch device memory. NULL is a no-op. */
+ls_status ls_prefix_destroy(ls_prefix_t h);
+
+/*
+ * ls_replay_fwd -- forward replay of one response against the resident prompt
+ * (review section 2-1 step 4, "serial policy replay"; section 3-2 (4)).
+ * For suffix row t (0 <= t < R) and query head h, with kv = h / g:
+ *     keys visible to (t, h):  all P prompt keys, then suffix keys 0..t (causal)
+ *     O[t,h,:]  = sum_j softmax_j(s * q[t,h,:] . k_j) v_j
+ *     lse[t,h]  = log sum_j exp(s * q[t,h,:] . k_j)        (natural log)
+ *   q       device bf16 THD [R, Hq, D]
+ *   k_suffix, v_suffix  device bf16 THD [R, Hkv, D]
+ *   o       device bf16 THD [R, Hq, D]   (written)
+ *   lse     device fp32 [R, Hq]          (written; ls_replay_bwd needs it)
+ *   R >= 1.  All pointers 16-byte aligned.
+ */
+ls_status ls_replay_fwd(ls_prefix_t h, int64_t R, const void* q, const void* k_suffix,
+                        const void* v_suffix, void* o, float* lse, void* stream);
+
+/* Bytes of device workspace ls_replay_bwd needs for a response of R tokens. */
+size_t ls_replay_bwd_workspace_bytes(ls_prefix_t h, int64_t R);
+
+/*
+ * ls_replay_bwd -- backward replay of one response (review section 2-1 step 4: "the
+ * suffix graph is released after its backward and only gradients are accumulated";
+ * section 2-2, the gradient decomposition at the prompt boundary z_P).
+ * With P = softmax(s Q K^T) recomputed from `lse`, dP = dO V^T, Delta = rowsum(dO * O),
+ * dS = P * (dP - Delta):
+ *     dq       = s dS K                    device bf16 THD [R, Hq, D]   (written)
+ *     dk_suffix= s dS^T Q  (suffix keys)   device bf16 THD [R, Hkv, D]  (written)
+ *     dv_suffix= P^T dO    (suffix keys)   device bf16 THD [R, Hkv, D]  (written)
+ *     dk_acc  += s dS^T Q  (prompt keys)   fp32, the handle's accumulator
+ *     dv_acc  += P^T dO    (prompt keys)   fp32, the handle's accumulator
+ * kv-head gradients sum over the g query heads of the group.  Inputs q, k_suffix,
+ * v_suffix, o (bf16 THD) and lse (fp32 [R, Hq]) are the ones given to / produced by
+ * ls_replay_fwd for this response; d_out is bf16 THD [R, Hq].
+ * The prompt accumulators are read-modified-written by exactly one CTA per tile, in
+ * stream order with other calls on the handle: no atomics, bitwise deterministic.
+ * workspace: device, >= ls_replay_bwd_workspace_bytes(h, R) bytes, 16-byte aligned.
+ */
+ls_status ls_replay_bwd(ls_prefix_t h, int64_t R, const void* q, const void* k_suffix,
+                        const void* v_suffix, const void* o, const float* lse,
+                        const void* d_out, void* dq, void* dk_suffix, void* dv_suffix,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of device workspace ls_grpo_loss needs for R token rows. */
+size_t ls_grpo_loss_workspace_bytes(int64_t R);
+
+/*
+ * ls_grpo_loss -- fused GRPO clipped-surrogate loss of one response (review section 1-1,
+ * equation L_policy).  Per token row t of logits x [R, V] with sampled id y_t:
+ *     lse   = log sum_v exp(x_v);  logp = x_y - lse;  rho = exp(logp - logp_old[t])
+ *     surr  = min(rho A, clip(rho, 1-eps, 1+eps) A)
+ *     *loss_accum += -(1/(G R)) sum_t surr          (fp64 device scalar, accumulated)
+ *     clip_mask[t] = 1 iff (A > 0 and rho > 1+eps) or (A < 0 and rho < 1-eps)
+ *     dlogits[t,v] = g_t (1[v = y_t] - exp(x_v - lse)),  g_t = -A rho [not clipped]/(G R)
+ *     logp_out[t]  = logp
+ *   logits   device bf16 [R, V];  ids device int32 [R], 0 <= id < V (an id outside that
+ *            range sets the device status and its row's outputs are zero)
+ *   logp_old device fp32 [R];  advantage A and eps (0 <= eps < 1) host scalars; G >= 1
+ *   loss_accum device double (accumulated, not cleared); dlogits device bf16 [R, V]
+ *   clip_mask device uint8 [R]; logp_out device fp32 [R] (may be NULL)
+ *   workspace device, >= ls_grpo_loss_workspace_bytes(R) bytes, 16-byte aligned.
+ * The token chain (lse combine, logp, rho, the clip decision, g, the loss terms) runs in
+ * fp64; the loss reduction is a fixed-order tree (deterministic).
+ */
+ls_status ls_grpo_loss(int64_t R, int64_t V, int32_t G, const void* logits, const int32_t* ids,
+                       const float* logp_old, double advantage, double eps, double* loss_accum,
+                       void* dlogits, uint8_t* clip_mask, float* logp_out, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/*
+ * ls_prefix_grad_finalize -- the group's one finalization (review section 2-1 step 5;
+ * section 3-2 (7)).  out = scale * acc for the prompt dK and dV accumulators.
+ *   dk_out, dv_out  device [P, Hkv, D], bf16 (out_is_fp32 = 0) or fp32 (out_is_fp32 = 1);
+ *                   both NULL scales the accumulators in place (fp32).
+ *   reset_acc       non-zero: zero the accumulators after reading them (not allowed with
+ *                   in-place output).
+ * On one GPU no collective is involved.
+ */
+ls_status ls_prefix_grad_finalize(ls_prefix_t h, float scale, void* dk_out, void* dv_out,
+                                  int out_is_fp32, int reset_acc, void* stream);
+
+/*
+ * Read (and clear) the device status word of the current device: synchronises `stream`,
+ * returns LS_OK, LS_ERR_TIMEOUT or LS_ERR_DEVICE_STATUS.  *bits (may be NULL) receives
+ * the raw word (1 = a bounded wait gave up, 2 = an index was outside its buffer).
+ */
+ls_status ls_get_device_status(void* stream, uint32_t* bits);
+
+const char* ls_status_string(ls_status s);
+
+/* Message of the last CUDA failure seen by this thread ("" if none). */
+const char* ls_last_error(void);
+
+/* Library version string, e.g. "0.1.0". */
+const char* ls_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LONGSTRAW_H */

@@ -6,9 +6,12 @@ it is missing.
 """
 __version__ = "0.1.0"
 
+_BINDING = ("Prefix", "grpo_loss", "grpo_loss_workspace_bytes", "device_status",
+            "LongStrawError", "library_path", "STATUS_NAMES")
+
 
 def __getattr__(name):
-    if name in ("Prefix", "grpo_loss", "lib", "LongStrawError", "library_path"):
+    if name in _BINDING:
         from . import _lib
         return getattr(_lib, name)
     raise AttributeError(name)

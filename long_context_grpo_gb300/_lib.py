@@ -1,0 +1,220 @@
+"""Thin ctypes binding over the C ABI in include/longstraw.h.
+
+Argument marshalling only: tensors are checked (device, dtype, shape, contiguity) and
+passed as raw pointers with torch's current CUDA stream; every step of the replay runs in
+the CUDA library.  PyTorch provides device memory and streams.  There is no fallback: if
+the library is missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+library_path = _build.LIB
+
+LS_OK = 0
+STATUS_NAMES = {
+    0: "LS_OK", 1: "LS_ERR_INVALID_ARGUMENT", 2: "LS_ERR_UNSUPPORTED", 3: "LS_ERR_NOT_PREPARED",
+    4: "LS_ERR_MISALIGNED", 5: "LS_ERR_CUDA", 6: "LS_ERR_TIMEOUT", 7: "LS_ERR_DEVICE_STATUS",
+    8: "LS_ERR_WORKSPACE", 9: "LS_ERR_WRONG_DEVICE",
+}
+
+
+class LongStrawError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = "%s failed: %s" % (where, STATUS_NAMES.get(status, str(status)))
+        if status == 5 and lib is not None:
+            msg += " (%s)" % lib.ls_last_error().decode()
+        super().__init__(msg)
+
+
+class PrefixDesc(ctypes.Structure):
+    _fields_ = [("P", ctypes.c_int64), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32),
+                ("D", ctypes.c_int32), ("softmax_scale", ctypes.c_float),
+                ("k_prefix", ctypes.c_void_p), ("v_prefix", ctypes.c_void_p),
+                ("dk_acc", ctypes.c_void_p), ("dv_acc", ctypes.c_void_p)]
+
+
+def _load():
+    if not os.path.exists(library_path):
+        raise RuntimeError("liblongstraw.so is not built (run long_context_grpo_gb300/build.py); "
+                           "there is no non-CUDA implementation")
+    L = ctypes.CDLL(library_path)
+    vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+    sig = {
+        "ls_prefix_prepare": (ctypes.c_int, [ctypes.POINTER(PrefixDesc), ctypes.POINTER(vp), vp]),
+        "ls_prefix_destroy": (ctypes.c_int, [vp]),
+        "ls_replay_fwd": (ctypes.c_int, [vp, i64, vp, vp, vp, vp, vp, vp]),
+        "ls_replay_bwd_workspace_bytes": (sz, [vp, i64]),
+        "ls_replay_bwd": (ctypes.c_int, [vp, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+        "ls_grpo_loss_workspace_bytes": (sz, [i64]),
+        "ls_grpo_loss": (ctypes.c_int, [i64, i64, i32, vp, vp, vp, ctypes.c_double,
+                                        ctypes.c_double, vp, vp, vp, vp, vp, sz, vp]),
+        "ls_prefix_grad_finalize": (ctypes.c_int, [vp, ctypes.c_float, vp, vp, ctypes.c_int,
+                                                   ctypes.c_int, vp]),
+        "ls_get_device_status": (ctypes.c_int, [vp, ctypes.POINTER(ctypes.c_uint32)]),
+        "ls_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        "ls_last_error": (ctypes.c_char_p, []),
+        "ls_version": (ctypes.c_char_p, []),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    return L
+
+
+lib = None
+
+
+def _lib():
+    global lib
+    if lib is None:
+        lib = _load()
+    return lib
+
+
+def _check(st: int, where: str):
+    if st != LS_OK:
+        raise LongStrawError(st, where)
+
+
+def _stream(stream=None) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _ptr(t, name, dtype, shape=None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+    return t.data_ptr()
+
+
+class Prefix:
+    """Resident prompt K/V of one attention layer and its fp32 gradient accumulators.
+
+    The tensors are borrowed: they must outlive the handle, and k/v are never written.
+    Creating the handle zeroes dk_acc / dv_acc on the current stream.
+    """
+
+    def __init__(self, k_prefix, v_prefix, dk_acc, dv_acc, Hq: int, softmax_scale: float = 0.0):
+        L = _lib()
+        P, Hkv, D = k_prefix.shape
+        self.P, self.Hq, self.Hkv, self.D = P, Hq, Hkv, D
+        self._keep = (k_prefix, v_prefix, dk_acc, dv_acc)
+        d = PrefixDesc(P, Hq, Hkv, D, softmax_scale,
+                       _ptr(k_prefix, "k_prefix", torch.bfloat16, (P, Hkv, D)),
+                       _ptr(v_prefix, "v_prefix", torch.bfloat16, (P, Hkv, D)),
+                       _ptr(dk_acc, "dk_acc", torch.float32, (P, Hkv, D)),
+                       _ptr(dv_acc, "dv_acc", torch.float32, (P, Hkv, D)))
+        h = ctypes.c_void_p()
+        _check(L.ls_prefix_prepare(ctypes.byref(d), ctypes.byref(h), _stream()), "ls_prefix_prepare")
+        self._h = h
+        self.dk_acc, self.dv_acc = dk_acc, dv_acc
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value is not None:
+            _check(_lib().ls_prefix_destroy(self._h), "ls_prefix_destroy")
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def fwd(self, q, k_suffix, v_suffix, o=None, lse=None):
+        R = q.shape[0]
+        if o is None:
+            o = torch.empty_like(q)
+        if lse is None:
+            lse = torch.empty((R, self.Hq), dtype=torch.float32, device=q.device)
+        _check(_lib().ls_replay_fwd(
+            self._h, R,
+            _ptr(q, "q", torch.bfloat16, (R, self.Hq, self.D)),
+            _ptr(k_suffix, "k_suffix", torch.bfloat16, (R, self.Hkv, self.D)),
+            _ptr(v_suffix, "v_suffix", torch.bfloat16, (R, self.Hkv, self.D)),
+            _ptr(o, "o", torch.bfloat16, (R, self.Hq, self.D)),
+            _ptr(lse, "lse", torch.float32, (R, self.Hq)), _stream()), "ls_replay_fwd")
+        return o, lse
+
+    def bwd_workspace_bytes(self, R: int) -> int:
+        return int(_lib().ls_replay_bwd_workspace_bytes(self._h, R))
+
+    def bwd(self, q, k_suffix, v_suffix, o, lse, d_out, dq=None, dk_suffix=None,
+            dv_suffix=None, workspace=None):
+        R = q.shape[0]
+        dq = torch.empty_like(q) if dq is None else dq
+        dk_suffix = torch.empty_like(k_suffix) if dk_suffix is None else dk_suffix
+        dv_suffix = torch.empty_like(v_suffix) if dv_suffix is None else dv_suffix
+        need = self.bwd_workspace_bytes(R)
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+        _check(_lib().ls_replay_bwd(
+            self._h, R,
+            _ptr(q, "q", torch.bfloat16, (R, self.Hq, self.D)),
+            _ptr(k_suffix, "k_suffix", torch.bfloat16, (R, self.Hkv, self.D)),
+            _ptr(v_suffix, "v_suffix", torch.bfloat16, (R, self.Hkv, self.D)),
+            _ptr(o, "o", torch.bfloat16, (R, self.Hq, self.D)),
+            _ptr(lse, "lse", torch.float32, (R, self.Hq)),
+            _ptr(d_out, "d_out", torch.bfloat16, (R, self.Hq, self.D)),
+            _ptr(dq, "dq", torch.bfloat16, (R, self.Hq, self.D)),
+            _ptr(dk_suffix, "dk_suffix", torch.bfloat16, (R, self.Hkv, self.D)),
+            _ptr(dv_suffix, "dv_suffix", torch.bfloat16, (R, self.Hkv, self.D)),
+            _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream()),
+            "ls_replay_bwd")
+        return dq, dk_suffix, dv_suffix
+
+    def finalize(self, scale: float = 1.0, dk_out=None, dv_out=None, out_fp32=False, reset=False):
+        shp = (self.P, self.Hkv, self.D)
+        dt = torch.float32 if out_fp32 else torch.bfloat16
+        _check(_lib().ls_prefix_grad_finalize(
+            self._h, scale, _ptr(dk_out, "dk_out", dt, shp), _ptr(dv_out, "dv_out", dt, shp),
+            1 if out_fp32 else 0, 1 if reset else 0, _stream()), "ls_prefix_grad_finalize")
+        return dk_out, dv_out
+
+
+def grpo_loss_workspace_bytes(R: int) -> int:
+    return int(_lib().ls_grpo_loss_workspace_bytes(R))
+
+
+def grpo_loss(logits, ids, logp_old, advantage: float, eps: float, G: int, loss_accum,
+              dlogits=None, clip_mask=None, logp_out=None, workspace=None):
+    """Adds this response's clipped-surrogate loss into loss_accum (fp64 [1]) and returns
+    (dlogits bf16 [R,V], clip_mask uint8 [R], logp fp32 [R])."""
+    R, V = logits.shape
+    dlogits = torch.empty_like(logits) if dlogits is None else dlogits
+    clip_mask = torch.empty((R,), dtype=torch.uint8, device=logits.device) if clip_mask is None else clip_mask
+    logp_out = torch.empty((R,), dtype=torch.float32, device=logits.device) if logp_out is None else logp_out
+    need = grpo_loss_workspace_bytes(R)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=logits.device)
+    _check(_lib().ls_grpo_loss(
+        R, V, G, _ptr(logits, "logits", torch.bfloat16, (R, V)),
+        _ptr(ids, "ids", torch.int32, (R,)), _ptr(logp_old, "logp_old", torch.float32, (R,)),
+        float(advantage), float(eps), _ptr(loss_accum, "loss_accum", torch.float64, (1,)),
+        _ptr(dlogits, "dlogits", torch.bfloat16, (R, V)),
+        _ptr(clip_mask, "clip_mask", torch.uint8, (R,)),
+        _ptr(logp_out, "logp_out", torch.float32, (R,)),
+        _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream()), "ls_grpo_loss")
+    return dlogits, clip_mask, logp_out
+
+
+def device_status():
+    """(status, bits) of the device status word; reading it clears it."""
+    bits = ctypes.c_uint32(0)
+    st = _lib().ls_get_device_status(_stream(), ctypes.byref(bits))
+    return st, bits.value

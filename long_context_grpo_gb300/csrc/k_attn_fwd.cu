@@ -1,0 +1,449 @@
+// K1: forward replay of one response against the resident prompt (LongStraw review,
+// dimensionstp.github.io "LongStraw", section 2-1 step 4 "serial policy replay" and
+// section 3-2 (4)): for every suffix row t and query head h,
+//   O[t,h] = softmax(s q_{t,h} . [K_prompt ; K_suffix[0..t]]) [V_prompt ; V_suffix[0..t]]
+//   LSE[t,h] = log sum exp(s q . k).
+//
+// GB300 design (one persistent CTA per SM, 384 threads):
+//   warp 0        TMA producer: two Q tiles per work unit, then K and V tiles (128 keys)
+//                 into separate 2-stage rings (prompt keys first, then the causal suffix).
+//   warp 1        one thread issues tcgen05.mma: S_q = Q_q K^T into TMEM (fp32, 128 cols)
+//                 and O_q += P_q V with P_q read back from TMEM (bf16, aliasing S_q).
+//   warp 2        allocates / frees the 512 TMEM columns.
+//   warps 4-7,    softmax warpgroups, one per Q tile; thread = TMEM lane = tile row.
+//   warps 8-11    Online softmax in log2 units with a lazy rescale: the running max only
+//                 moves when a tile's max exceeds it by more than 2^8, and only then is
+//                 the O row in TMEM rescaled.
+// A work unit is (kv head, pair of 128-row Q tiles); each 128-row tile packs qt = 128/g
+// consecutive queries x the g query heads that share the kv head, so one K/V tile feeds
+// 2 x 128 rows of MMA.  Units are ordered kv-head-major so the CTAs running at the same
+// time stream the same prompt K/V through L2.
+// Every wait is bounded; on a timeout the CTA records it in the status word, drains its
+// in-flight copies and MMAs, frees TMEM and exits.
+#include "ls_internal.h"
+#include "ptx.cuh"
+
+namespace ls {
+namespace {
+
+constexpr int kThreads = 384;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleLog2 = 8.0f;
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kTile = 128 * D * 2;          // bytes of a 128-row bf16 tile
+  static constexpr int kNK = (D == 128) ? 2 : 4;     // K ring stages
+  static constexpr int kNV = (D == 128) ? 2 : 4;     // V ring stages
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = 2 * kTile;
+  static constexpr int kOffV = kOffK + kNK * kTile;
+  static constexpr int kOffBar = kOffV + kNV * kTile;
+  // barriers: q_full, q_empty, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV],
+  //           s_full[2], p_full[2], o_done[2], o_free[2], drain
+  static constexpr int kBarQFull = 0, kBarQEmpty = 1, kBarKFull = 2;
+  static constexpr int kBarKEmpty = kBarKFull + kNK;
+  static constexpr int kBarVFull = kBarKEmpty + kNK;
+  static constexpr int kBarVEmpty = kBarVFull + kNV;
+  static constexpr int kBarSFull = kBarVEmpty + kNV;
+  static constexpr int kBarPFull = kBarSFull + 2;
+  static constexpr int kBarODone = kBarPFull + 2;
+  static constexpr int kBarOFree = kBarODone + 2;
+  static constexpr int kBarDrain = kBarOFree + 2;
+  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kSmem = kOffBar + kNumBars * 8 + 16 + 1024;
+  // TMEM columns: S_q at 128 q (P_q aliases its first 64 columns), O_q at 256 + D q
+  __host__ __device__ static constexpr uint32_t col_s(int q) { return 128u * q; }
+  __host__ __device__ static constexpr uint32_t col_o(int q) { return 256u + D * q; }
+};
+
+struct Unit {
+  int kv;
+  int t0;        // first query of Q tile 0
+  bool has1;     // Q tile 1 exists
+  int n_pt;      // prompt key tiles
+  int n_kt;      // total key tiles
+};
+
+__device__ __forceinline__ Unit make_unit(int u, const AttnShape& sh, int n_pairs) {
+  Unit w;
+  w.kv = u / n_pairs;
+  const int pair = u - w.kv * n_pairs;
+  const int n_qt = static_cast<int>((sh.R + sh.qt - 1) / sh.qt);
+  w.t0 = pair * 2 * sh.qt;
+  w.has1 = (2 * pair + 1) < n_qt;
+  int t_end = w.t0 + (w.has1 ? 2 : 1) * sh.qt;
+  if (t_end > sh.R) t_end = static_cast<int>(sh.R);
+  w.n_pt = static_cast<int>((sh.P + 127) / 128);
+  w.n_kt = w.n_pt + (t_end + 127) / 128;
+  return w;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_kp,
+                    const __grid_constant__ CUtensorMap tm_vp,
+                    const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_ks,
+                    const __grid_constant__ CUtensorMap tm_vs, const AttnShape sh,
+                    uint16_t* __restrict__ o_out, float* __restrict__ lse_out,
+                    uint32_t* status) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n_pairs = static_cast<int>(((sh.R + sh.qt - 1) / sh.qt + 1) / 2);
+  const int n_units = sh.Hkv * n_pairs;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bars[C::kBarQFull], 1);
+    mbar_init(&bars[C::kBarQEmpty], 1);
+    for (int i = 0; i < C::kNK; ++i) {
+      mbar_init(&bars[C::kBarKFull + i], 1);
+      mbar_init(&bars[C::kBarKEmpty + i], 1);
+    }
+    for (int i = 0; i < C::kNV; ++i) {
+      mbar_init(&bars[C::kBarVFull + i], 1);
+      mbar_init(&bars[C::kBarVEmpty + i], 1);
+    }
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(&bars[C::kBarSFull + q], 1);
+      mbar_init(&bars[C::kBarPFull + q], 128);
+      mbar_init(&bars[C::kBarODone + q], 1);
+      mbar_init(&bars[C::kBarOFree + q], 128);
+    }
+    mbar_init(&bars[C::kBarDrain], 1);
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    __syncwarp();
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  volatile int* vabort = &abort_flag;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_kp);
+      tma_prefetch_desc(&tm_vp);
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_ks);
+      tma_prefetch_desc(&tm_vs);
+      uint32_t kit = 0, vit = 0, uc = 0;
+      uint32_t k_issued[C::kNK > 0 ? C::kNK : 1] = {};
+      uint32_t v_issued[C::kNV > 0 ? C::kNV : 1] = {};
+      bool ok = true;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
+        const Unit w = make_unit(u, sh, n_pairs);
+        if (uc > 0) ok = mbar_wait(&bars[C::kBarQEmpty], (uc - 1) & 1u, status);
+        if (!ok) break;
+        const int nq = w.has1 ? 2 : 1;
+        mbar_arrive_expect_tx(&bars[C::kBarQFull],
+                              static_cast<uint32_t>(nq * C::kBoxes * 128 * sh.g * sh.qt));
+        for (int q = 0; q < nq; ++q)
+          for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_3d(smem + C::kOffQ + q * C::kTile + b * 16384, &tm_q, &bars[C::kBarQFull],
+                        64 * b, w.kv * sh.g, w.t0 + q * sh.qt);
+        for (int j = 0; j < w.n_kt && ok; ++j) {
+          const bool pre = j < w.n_pt;
+          const int key0 = pre ? 128 * j : 128 * (j - w.n_pt);
+          {
+            const uint32_t s = kit % C::kNK;
+            if (kit >= static_cast<uint32_t>(C::kNK))
+              ok = mbar_wait(&bars[C::kBarKEmpty + s], ((kit / C::kNK) - 1) & 1u, status);
+            if (!ok) break;
+            mbar_arrive_expect_tx(&bars[C::kBarKFull + s], C::kTile);
+            for (int b = 0; b < C::kBoxes; ++b)
+              tma_load_3d(smem + C::kOffK + s * C::kTile + b * 16384, pre ? &tm_kp : &tm_ks,
+                          &bars[C::kBarKFull + s], 64 * b, w.kv, key0);
+            ++k_issued[s];
+            ++kit;
+          }
+          {
+            const uint32_t s = vit % C::kNV;
+            if (vit >= static_cast<uint32_t>(C::kNV))
+              ok = mbar_wait(&bars[C::kBarVEmpty + s], ((vit / C::kNV) - 1) & 1u, status);
+            if (!ok) break;
+            mbar_arrive_expect_tx(&bars[C::kBarVFull + s], C::kTile);
+            for (int b = 0; b < C::kBoxes; ++b)
+              tma_load_3d(smem + C::kOffV + s * C::kTile + b * 16384, pre ? &tm_vp : &tm_vs,
+                          &bars[C::kBarVFull + s], 64 * b, w.kv, key0);
+            ++v_issued[s];
+            ++vit;
+          }
+        }
+      }
+      if (!ok) {
+        *vabort = 1;
+        // drain this thread's own copies still in flight before the CTA may exit
+        for (int s = 0; s < C::kNK; ++s)
+          if (k_issued[s]) mbar_wait_ns(&bars[C::kBarKFull + s], (k_issued[s] - 1) & 1u, 200000000ull);
+        for (int s = 0; s < C::kNV; ++s)
+          if (v_issued[s]) mbar_wait_ns(&bars[C::kBarVFull + s], (v_issued[s] - 1) & 1u, 200000000ull);
+        mbar_wait_ns(&bars[C::kBarQFull], (uc) & 1u, 200000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t kIdPV = idesc_bf16(128, D, false, true);
+      const uint32_t sQ = smem_u32(smem + C::kOffQ);
+      const uint32_t sK = smem_u32(smem + C::kOffK);
+      const uint32_t sV = smem_u32(smem + C::kOffV);
+      uint32_t kit = 0, vit = 0, uc = 0;
+      uint32_t pph[2] = {0u, 0u};    // p_full phase per tile
+      uint32_t uq[2] = {0u, 0u};     // units processed per tile
+      bool ok = true;
+
+      auto issue_s = [&](int q, uint32_t kstage) {
+        const uint32_t qa = sQ + q * C::kTile;
+        const uint32_t ka = sK + kstage * C::kTile;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_bf16_ss(tmem + C::col_s(q), smem_desc(qa + off, 16, 1024),
+                      smem_desc(ka + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int q, uint32_t vstage, bool acc) {
+        const uint32_t va = sV + vstage * C::kTile;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16_ts(tmem + C::col_o(q), tmem + C::col_s(q) + kk * 8,
+                      smem_desc(va + kk * 2048, 16384, 1024), kIdPV, (acc || kk > 0) ? 1u : 0u);
+      };
+
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
+        const Unit w = make_unit(u, sh, n_pairs);
+        const int nq = w.has1 ? 2 : 1;
+        ok = mbar_wait(&bars[C::kBarQFull], uc & 1u, status, vabort);
+        if (!ok) break;
+        tc_fence_after();
+        // S_q(0)
+        uint32_t ks = kit % C::kNK;
+        ok = mbar_wait(&bars[C::kBarKFull + ks], (kit / C::kNK) & 1u, status, vabort);
+        if (!ok) break;
+        tc_fence_after();
+        for (int q = 0; q < nq; ++q) {
+          issue_s(q, ks);
+          mma_commit(&bars[C::kBarSFull + q]);
+        }
+        mma_commit(&bars[C::kBarKEmpty + ks]);
+        ++kit;
+        for (int j = 0; j < w.n_kt && ok; ++j) {
+          const uint32_t vs = vit % C::kNV;
+          ok = mbar_wait(&bars[C::kBarVFull + vs], (vit / C::kNV) & 1u, status, vabort);
+          if (!ok) break;
+          const bool more = (j + 1) < w.n_kt;
+          uint32_t ks_next = kit % C::kNK;
+          for (int q = 0; q < nq && ok; ++q) {
+            ok = mbar_wait(&bars[C::kBarPFull + q], pph[q], status, vabort);
+            if (!ok) break;
+            pph[q] ^= 1u;
+            if (j == 0 && uq[q] > 0) {
+              ok = mbar_wait(&bars[C::kBarOFree + q], (uq[q] - 1) & 1u, status, vabort);
+              if (!ok) break;
+            }
+            tc_fence_after();
+            issue_pv(q, vs, j > 0);
+            if (!more) mma_commit(&bars[C::kBarODone + q]);
+            if (more) {
+              if (q == 0) {
+                ok = mbar_wait(&bars[C::kBarKFull + ks_next], (kit / C::kNK) & 1u, status, vabort);
+                if (!ok) break;
+                tc_fence_after();
+              }
+              issue_s(q, ks_next);
+              mma_commit(&bars[C::kBarSFull + q]);
+            }
+          }
+          if (!ok) break;
+          if (more) {
+            mma_commit(&bars[C::kBarKEmpty + ks_next]);
+            ++kit;
+          }
+          mma_commit(&bars[C::kBarVEmpty + vs]);
+          ++vit;
+        }
+        if (!ok) break;
+        for (int q = 0; q < nq; ++q) ++uq[q];
+        if (u + static_cast<int>(gridDim.x) < n_units) mma_commit(&bars[C::kBarQEmpty]);
+      }
+      if (!ok) *vabort = 1;
+      // drain: every MMA (and the arrivals committed behind it) has landed before exit
+      mma_commit(&bars[C::kBarDrain]);
+      mbar_wait_ns(&bars[C::kBarDrain], 0u, ok ? LS_WAIT_LIMIT_NS : 200000000ull);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax warpgroups
+    const int q = (warp - 4) >> 2;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t colS = C::col_s(q), colO = C::col_o(q);
+    const float c2 = sh.scale * kLog2e;
+    uint32_t sph = 0u, uq = 0u;
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      const Unit w = make_unit(u, sh, n_pairs);
+      if (q == 1 && !w.has1) continue;
+      const int t = w.t0 + q * sh.qt + row / sh.g;
+      float m_run = -INFINITY, l = 0.0f;
+      for (int j = 0; j < w.n_kt; ++j) {
+        ok = mbar_wait(&bars[C::kBarSFull + q], sph, status, vabort);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        sph ^= 1u;
+        tc_fence_after();
+        uint32_t sv[4][32];
+        tmem_ld32(lane_base + colS + 0, sv[0]);
+        tmem_ld32(lane_base + colS + 32, sv[1]);
+        tmem_ld32(lane_base + colS + 64, sv[2]);
+        tmem_ld32(lane_base + colS + 96, sv[3]);
+        tmem_ld_wait();
+        // valid key columns of this row in this tile
+        int lim = 128;
+        if (j < w.n_pt) {
+          const int64_t rem = sh.P - 128ll * j;
+          if (rem < 128) lim = static_cast<int>(rem);
+        } else {
+          const int k0 = 128 * (j - w.n_pt);
+          const int v = t - k0 + 1;
+          lim = v < 0 ? 0 : (v > 128 ? 128 : v);
+        }
+        float mx = -INFINITY;
+        if (lim < 128) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c >= lim) sv[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+        }
+#pragma unroll
+        for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sv[c >> 5][c & 31]));
+        const float mt = mx * c2;
+        float factor = 1.0f;
+        bool resc = false;
+        if (m_run == -INFINITY) {
+          m_run = mt;
+        } else if (mt > m_run + kRescaleLog2) {
+          factor = ex2_approx(m_run - mt);
+          l *= factor;
+          m_run = mt;
+          resc = true;
+        }
+        const float neg_m = (m_run == -INFINITY) ? 0.0f : -m_run;
+        float rs = 0.0f;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t pw[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int c = half * 64 + 2 * i;
+            const float p0 = ex2_approx(fmaf(__uint_as_float(sv[c >> 5][c & 31]), c2, neg_m));
+            const float p1 =
+                ex2_approx(fmaf(__uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]), c2, neg_m));
+            rs += p0 + p1;
+            pw[i] = pack_bf16x2(p0, p1);
+          }
+          tmem_st32(lane_base + colS + half * 32, pw);
+        }
+        l += rs;
+        if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t ov[32];
+            tmem_ld32(lane_base + colO + cc * 32, ov);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * factor);
+            tmem_st32(lane_base + colO + cc * 32, ov);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars[C::kBarPFull + q]);
+      }
+      if (!ok) break;
+      // epilogue: O / l -> bf16, LSE
+      ok = mbar_wait(&bars[C::kBarODone + q], uq & 1u, status, vabort);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const bool valid = (row < sh.g * sh.qt) && (t < sh.R);
+      const int h = w.kv * sh.g + row % sh.g;
+      const float inv_l = (l > 0.0f) ? 1.0f / l : 0.0f;
+      uint16_t* orow = o_out + (static_cast<int64_t>(t) * sh.Hq + h) * D;
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t ov[32];
+        tmem_ld32(lane_base + colO + cc * 32, ov);
+        tmem_ld_wait();
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint4 pk;
+            pk.x = pack_bf16x2(__uint_as_float(ov[8 * i + 0]) * inv_l, __uint_as_float(ov[8 * i + 1]) * inv_l);
+            pk.y = pack_bf16x2(__uint_as_float(ov[8 * i + 2]) * inv_l, __uint_as_float(ov[8 * i + 3]) * inv_l);
+            pk.z = pack_bf16x2(__uint_as_float(ov[8 * i + 4]) * inv_l, __uint_as_float(ov[8 * i + 5]) * inv_l);
+            pk.w = pack_bf16x2(__uint_as_float(ov[8 * i + 6]) * inv_l, __uint_as_float(ov[8 * i + 7]) * inv_l);
+            dst[i] = pk;
+          }
+        }
+      }
+      if (valid) lse_out[static_cast<int64_t>(t) * sh.Hq + h] = (m_run + __log2f(l)) * kLn2;
+      tc_fence_before();
+      mbar_arrive(&bars[C::kBarOFree + q]);
+      ++uq;
+    }
+    if (!ok) *vabort = 1;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t s) {
+  using C = FwdCfg<D>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int64_t n_qt = (a.sh.R + a.sh.qt - 1) / a.sh.qt;
+  const int64_t n_units = static_cast<int64_t>(a.sh.Hkv) * ((n_qt + 1) / 2);
+  int grid = num_sms();
+  if (n_units < grid) grid = static_cast<int>(n_units);
+  attn_fwd_kernel<D><<<grid, kThreads, C::kSmem, s>>>(*a.tm_kp, *a.tm_vp, a.tm_q, a.tm_ks,
+                                                      a.tm_vs, a.sh, a.o, a.lse, a.status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t s) {
+  return a.sh.D == 128 ? launch_fwd_d<128>(a, s) : launch_fwd_d<64>(a, s);
+}
+
+}  // namespace ls

@@ -1,0 +1,151 @@
+// Bandwidth kernels around the replay:
+//   K0 zero_f32        zero the fp32 prompt-gradient accumulators (prompt capture hand-off)
+//   K7 finalize        out = scale * acc (bf16 or fp32), optionally zeroing acc: the group's
+//                      one finalization (LongStraw review, section 2-1 step 5)
+//   K2 bwd_prep        Delta[t,h] = sum_d dO[t,h,d] O[t,h,d], the row term of the softmax
+//                      backward dS = P * (dP - Delta), packed with LSE by 64-row sub-tile
+// All use 128-bit accesses on a grid sized to the SM count.
+#include "ls_internal.h"
+
+namespace ls {
+namespace {
+
+constexpr int kThreads = 256;
+
+__global__ void __launch_bounds__(kThreads) zero_f32_kernel(float4* p, size_t n4, float* tail,
+                                                           size_t ntail) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * kThreads;
+  for (size_t i = blockIdx.x * static_cast<size_t>(kThreads) + threadIdx.x; i < n4; i += stride)
+    p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (blockIdx.x == 0 && threadIdx.x < ntail) tail[threadIdx.x] = 0.f;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <bool kOutF32>
+__global__ void __launch_bounds__(kThreads) finalize_kernel(float4* acc, void* out, size_t n4,
+                                                           float scale, int reset) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * kThreads;
+  for (size_t i = blockIdx.x * static_cast<size_t>(kThreads) + threadIdx.x; i < n4; i += stride) {
+    float4 a = __ldcs(acc + i);
+    a.x *= scale; a.y *= scale; a.z *= scale; a.w *= scale;
+    if (kOutF32) {
+      __stcs(reinterpret_cast<float4*>(out) + i, a);
+    } else {
+      uint2 b;
+      b.x = bf16x2_rn(a.x, a.y);
+      b.y = bf16x2_rn(a.z, a.w);
+      __stcs(reinterpret_cast<uint2*>(out) + i, b);
+    }
+    if (reset) __stcs(acc + i, make_float4(0.f, 0.f, 0.f, 0.f));
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) scale_kernel(float4* acc, size_t n4, float scale) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * kThreads;
+  for (size_t i = blockIdx.x * static_cast<size_t>(kThreads) + threadIdx.x; i < n4; i += stride) {
+    float4 a = acc[i];
+    a.x *= scale; a.y *= scale; a.z *= scale; a.w *= scale;
+    acc[i] = a;
+  }
+}
+
+// One warp per 64-row sub-tile slot (kv, i, r): row r of sub-tile i packs query
+// t = i * qt64 + r / g and head h = kv * g + r % g.  Valid rows get
+// (LSE * log2 e, Delta = sum_d dO * O); padding rows and rows past R get (+inf, 0).
+__global__ void __launch_bounds__(kThreads) bwd_prep_kernel(const uint4* o, const uint4* d_out,
+                                                           const float* lse, float2* rowstats,
+                                                           AttnShape sh, int qt64, int64_t n_q64) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps_total = static_cast<int64_t>(gridDim.x) * (kThreads / 32);
+  const int per_row = sh.D / 8;   // 8 or 16 lanes, 8 bf16 each
+  const int64_t slots = static_cast<int64_t>(sh.Hkv) * n_q64 * 64;
+  for (int64_t sidx = blockIdx.x * static_cast<int64_t>(kThreads / 32) + (threadIdx.x >> 5);
+       sidx < slots; sidx += warps_total) {
+    const int64_t kv = sidx / (n_q64 * 64);
+    const int64_t rem = sidx - kv * n_q64 * 64;
+    const int64_t i = rem >> 6;
+    const int r = static_cast<int>(rem & 63);
+    const int64_t t = i * qt64 + r / sh.g;
+    const int64_t h = kv * sh.g + r % sh.g;
+    const bool valid = (r < sh.g * qt64) && (t < sh.R);
+    float acc = 0.f;
+    if (valid && lane < per_row) {
+      const int64_t row = t * sh.Hq + h;
+      const uint4 a = __ldcs(o + row * per_row + lane);
+      const uint4 b = __ldcs(d_out + row * per_row + lane);
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+      const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        acc = fmaf(__uint_as_float(aw[k] << 16), __uint_as_float(bw[k] << 16), acc);
+        acc = fmaf(__uint_as_float(aw[k] & 0xFFFF0000u), __uint_as_float(bw[k] & 0xFFFF0000u), acc);
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) {
+      float2 v;
+      if (valid) {
+        v.x = lse[t * sh.Hq + h] * 1.4426950408889634f;
+        v.y = acc;
+      } else {
+        v.x = INFINITY;
+        v.y = 0.f;
+      }
+      rowstats[sidx] = v;
+    }
+  }
+}
+
+unsigned grid_for(size_t work_items) {
+  const size_t per_block = kThreads;
+  size_t blocks = (work_items + per_block - 1) / per_block;
+  const size_t cap = static_cast<size_t>(num_sms()) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return static_cast<unsigned>(blocks);
+}
+
+}  // namespace
+
+cudaError_t launch_zero_f32(float* p, size_t n, cudaStream_t s) {
+  const size_t n4 = n / 4, ntail = n % 4;
+  zero_f32_kernel<<<grid_for(n4), kThreads, 0, s>>>(reinterpret_cast<float4*>(p), n4,
+                                                     p + n4 * 4, ntail);
+  return cudaGetLastError();
+}
+
+// n is a multiple of 4 (P * Hkv * D with D in {64, 128}).
+cudaError_t launch_finalize(const float* acc, void* out, size_t n, float scale, int out_fp32,
+                            int reset, cudaStream_t s) {
+  const size_t n4 = n / 4;
+  float4* a4 = reinterpret_cast<float4*>(const_cast<float*>(acc));
+  if (out_fp32)
+    finalize_kernel<true><<<grid_for(n4), kThreads, 0, s>>>(a4, out, n4, scale, reset);
+  else
+    finalize_kernel<false><<<grid_for(n4), kThreads, 0, s>>>(a4, out, n4, scale, reset);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scale_inplace(float* acc, size_t n, float scale, cudaStream_t s) {
+  const size_t n4 = n / 4;
+  scale_kernel<<<grid_for(n4), kThreads, 0, s>>>(reinterpret_cast<float4*>(acc), n4, scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_prep(const uint16_t* o, const uint16_t* d_out, const float* lse,
+                            float2* rowstats, const AttnShape& sh, int qt64, cudaStream_t s) {
+  const int64_t n_q64 = (sh.R + qt64 - 1) / qt64;
+  const size_t slots = static_cast<size_t>(sh.Hkv) * n_q64 * 64;
+  bwd_prep_kernel<<<grid_for(slots * 32), kThreads, 0, s>>>(
+      reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(d_out), lse, rowstats, sh,
+      qt64, n_q64);
+  return cudaGetLastError();
+}
+
+}  // namespace ls

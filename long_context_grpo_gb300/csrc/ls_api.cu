@@ -1,0 +1,442 @@
+// Host side of the C ABI declared in include/longstraw.h: argument validation, TMA
+// descriptor encoding, launch sequencing on the caller's stream and error mapping.
+// The library allocates no device memory; the only device-resident state it owns is the
+// 4-byte status word below (one per device, a module global).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "../../include/longstraw.h"
+#include "ls_internal.h"
+#include "ptx.cuh"
+
+namespace ls {
+
+__device__ uint32_t g_status_word = 0u;
+
+namespace {
+
+constexpr uint32_t kMagic = 0x4c535046u;  // "LSPF"
+constexpr int kMaxDevices = 64;
+
+thread_local char t_last_error[256] = "";
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+std::mutex g_dev_mu;
+uint32_t* g_status_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+
+ls_status cuda_fail(cudaError_t e, const char* what) {
+  snprintf(t_last_error, sizeof(t_last_error), "%s: %s", what, cudaGetErrorString(e));
+  return LS_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0u; }
+bool aligned_n(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0u; }
+
+ls_status current_device(int* dev) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (*dev < 0 || *dev >= kMaxDevices) return LS_ERR_UNSUPPORTED;
+  return LS_OK;
+}
+
+// Address of this device's status word (looked up once per device, with it current).
+ls_status status_ptr(int dev, uint32_t** out) {
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (g_status_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_status_word);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
+    g_status_ptr[dev] = static_cast<uint32_t*>(p);
+  }
+  *out = g_status_ptr[dev];
+  return LS_OK;
+}
+
+ls_status check_stream(void* stream, int dev) {
+  if (stream == nullptr) return LS_OK;
+  int sdev = -1;
+  cudaError_t e = cudaStreamGetDevice(static_cast<cudaStream_t>(stream), &sdev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamGetDevice");
+  return sdev == dev ? LS_OK : LS_ERR_WRONG_DEVICE;
+}
+
+ls_status get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (g_encode == nullptr) {
+    snprintf(t_last_error, sizeof(t_last_error), "cuTensorMapEncodeTiled unavailable");
+    return LS_ERR_CUDA;
+  }
+  return LS_OK;
+}
+
+// 3-D bf16 THD tensor [T][H][D] with a {64, hbox, tbox} box and 128-byte swizzle.
+ls_status encode_thd(CUtensorMap* m, const void* base, int64_t T, int H, int D, int hbox,
+                     int tbox) {
+  ls_status st = get_encoder();
+  if (st != LS_OK) return st;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(T)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2u,
+                           static_cast<cuuint64_t>(H) * static_cast<cuuint64_t>(D) * 2u};
+  cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(hbox), static_cast<cuuint32_t>(tbox)};
+  cuuint32_t es[3] = {1u, 1u, 1u};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(t_last_error, sizeof(t_last_error), "cuTensorMapEncodeTiled failed (%d)",
+             static_cast<int>(r));
+    return LS_ERR_CUDA;
+  }
+  return LS_OK;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+int num_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (g_num_sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    g_num_sms[dev] = n;
+  }
+  return g_num_sms[dev];
+}
+
+}  // namespace ls
+
+struct ls_prefix_s {
+  uint32_t magic;
+  int device;
+  ls::AttnShape shape;    // R unused here
+  const void* k_prefix;
+  const void* v_prefix;
+  float* dk_acc;
+  float* dv_acc;
+  CUtensorMap tm_k;     // box {64, 1, 128}: forward and dK/dV key tiles
+  CUtensorMap tm_v;
+  CUtensorMap tm_k64;   // box {64, 1, 64}: dQ key steps
+  CUtensorMap tm_v64;
+};
+
+namespace {
+
+using namespace ls;
+
+ls_status check_handle(ls_prefix_t h) {
+  if (h == nullptr || h->magic != kMagic) return LS_ERR_NOT_PREPARED;
+  return LS_OK;
+}
+
+ls_status enter(ls_prefix_t h, void* stream, uint32_t** status) {
+  int dev = 0;
+  ls_status st = current_device(&dev);
+  if (st != LS_OK) return st;
+  if (h != nullptr && dev != h->device) return LS_ERR_WRONG_DEVICE;
+  st = check_stream(stream, dev);
+  if (st != LS_OK) return st;
+  return status_ptr(dev, status);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ls_version(void) { return "0.1.0"; }
+
+const char* ls_last_error(void) { return t_last_error; }
+
+const char* ls_status_string(ls_status s) {
+  switch (s) {
+    case LS_OK: return "ok";
+    case LS_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case LS_ERR_UNSUPPORTED: return "unsupported shape";
+    case LS_ERR_NOT_PREPARED: return "prefix handle not prepared";
+    case LS_ERR_MISALIGNED: return "device pointer not 16-byte aligned";
+    case LS_ERR_CUDA: return "CUDA error";
+    case LS_ERR_TIMEOUT: return "device wait timed out";
+    case LS_ERR_DEVICE_STATUS: return "device-side check failed";
+    case LS_ERR_WORKSPACE: return "workspace missing or too small";
+    case LS_ERR_WRONG_DEVICE: return "wrong device";
+  }
+  return "unknown status";
+}
+
+ls_status ls_prefix_prepare(const ls_prefix_desc* d, ls_prefix_t* out, void* stream) {
+  if (d == nullptr || out == nullptr) return LS_ERR_INVALID_ARGUMENT;
+  if (d->k_prefix == nullptr || d->v_prefix == nullptr || d->dk_acc == nullptr ||
+      d->dv_acc == nullptr)
+    return LS_ERR_INVALID_ARGUMENT;
+  if (d->P < 1 || d->Hq < 1 || d->Hkv < 1) return LS_ERR_INVALID_ARGUMENT;
+  if (!(d->softmax_scale >= 0.0f) || !std::isfinite(d->softmax_scale))
+    return LS_ERR_INVALID_ARGUMENT;
+  if (d->D != 64 && d->D != 128) return LS_ERR_UNSUPPORTED;
+  if (d->Hq % d->Hkv != 0) return LS_ERR_UNSUPPORTED;
+  const int g = d->Hq / d->Hkv;
+  if (g > 16) return LS_ERR_UNSUPPORTED;
+  if (d->P >= (int64_t(1) << 31)) return LS_ERR_UNSUPPORTED;
+  if (!aligned16(d->k_prefix) || !aligned16(d->v_prefix) || !aligned16(d->dk_acc) ||
+      !aligned16(d->dv_acc))
+    return LS_ERR_MISALIGNED;
+
+  uint32_t* status = nullptr;
+  ls_status st = enter(nullptr, stream, &status);
+  if (st != LS_OK) return st;
+  int dev = 0;
+  cudaGetDevice(&dev);
+
+  ls_prefix_s* h = new (std::nothrow) ls_prefix_s();
+  if (h == nullptr) return LS_ERR_INVALID_ARGUMENT;
+  h->device = dev;
+  h->shape.P = d->P;
+  h->shape.R = 0;
+  h->shape.Hq = d->Hq;
+  h->shape.Hkv = d->Hkv;
+  h->shape.D = d->D;
+  h->shape.g = g;
+  h->shape.qt = 128 / g;
+  h->shape.scale = d->softmax_scale > 0.0f ? d->softmax_scale
+                                           : 1.0f / std::sqrt(static_cast<float>(d->D));
+  h->k_prefix = d->k_prefix;
+  h->v_prefix = d->v_prefix;
+  h->dk_acc = d->dk_acc;
+  h->dv_acc = d->dv_acc;
+  st = encode_thd(&h->tm_k, d->k_prefix, d->P, d->Hkv, d->D, 1, 128);
+  if (st == LS_OK) st = encode_thd(&h->tm_v, d->v_prefix, d->P, d->Hkv, d->D, 1, 128);
+  if (st == LS_OK) st = encode_thd(&h->tm_k64, d->k_prefix, d->P, d->Hkv, d->D, 1, 64);
+  if (st == LS_OK) st = encode_thd(&h->tm_v64, d->v_prefix, d->P, d->Hkv, d->D, 1, 64);
+  if (st != LS_OK) {
+    delete h;
+    return st;
+  }
+  const size_t n = static_cast<size_t>(d->P) * d->Hkv * d->D;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_zero_f32(d->dk_acc, n, s);
+  if (e == cudaSuccess) e = launch_zero_f32(d->dv_acc, n, s);
+  if (e != cudaSuccess) {
+    delete h;
+    return cuda_fail(e, "prefix accumulator zeroing");
+  }
+  h->magic = kMagic;
+  *out = h;
+  return LS_OK;
+}
+
+ls_status ls_prefix_destroy(ls_prefix_t h) {
+  if (h == nullptr) return LS_OK;
+  if (h->magic != kMagic) return LS_ERR_NOT_PREPARED;
+  h->magic = 0;
+  delete h;
+  return LS_OK;
+}
+
+ls_status ls_replay_fwd(ls_prefix_t h, int64_t R, const void* q, const void* k_suffix,
+                        const void* v_suffix, void* o, float* lse, void* stream) {
+  ls_status st = check_handle(h);
+  if (st != LS_OK) return st;
+  if (q == nullptr || k_suffix == nullptr || v_suffix == nullptr || o == nullptr ||
+      lse == nullptr)
+    return LS_ERR_INVALID_ARGUMENT;
+  if (R < 1) return LS_ERR_INVALID_ARGUMENT;
+  if (R >= (int64_t(1) << 31)) return LS_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_suffix) || !aligned16(v_suffix) || !aligned16(o) ||
+      !aligned_n(lse, 4))
+    return LS_ERR_MISALIGNED;
+  uint32_t* status = nullptr;
+  st = enter(h, stream, &status);
+  if (st != LS_OK) return st;
+
+  FwdArgs a{};
+  a.sh = h->shape;
+  a.sh.R = R;
+  a.tm_kp = &h->tm_k;
+  a.tm_vp = &h->tm_v;
+  const AttnShape& sh = a.sh;
+  st = encode_thd(&a.tm_q, q, R, sh.Hq, sh.D, sh.g, sh.qt);
+  if (st == LS_OK) st = encode_thd(&a.tm_ks, k_suffix, R, sh.Hkv, sh.D, 1, 128);
+  if (st == LS_OK) st = encode_thd(&a.tm_vs, v_suffix, R, sh.Hkv, sh.D, 1, 128);
+  if (st != LS_OK) return st;
+  a.o = static_cast<uint16_t*>(o);
+  a.lse = lse;
+  a.status = status;
+  cudaError_t e = launch_attn_fwd(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? LS_OK : cuda_fail(e, "replay forward launch");
+}
+
+size_t ls_replay_bwd_workspace_bytes(ls_prefix_t h, int64_t R) {
+  if (check_handle(h) != LS_OK || R < 1) return 0;
+  const int64_t qt64 = 64 / h->shape.g;
+  const int64_t n_q64 = (R + qt64 - 1) / qt64;
+  return align_up(static_cast<size_t>(h->shape.Hkv) * n_q64 * 64 * sizeof(float2), 256);
+}
+
+ls_status ls_replay_bwd(ls_prefix_t h, int64_t R, const void* q, const void* k_suffix,
+                        const void* v_suffix, const void* o, const float* lse,
+                        const void* d_out, void* dq, void* dk_suffix, void* dv_suffix,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  ls_status st = check_handle(h);
+  if (st != LS_OK) return st;
+  if (q == nullptr || k_suffix == nullptr || v_suffix == nullptr || o == nullptr ||
+      lse == nullptr || d_out == nullptr || dq == nullptr || dk_suffix == nullptr ||
+      dv_suffix == nullptr)
+    return LS_ERR_INVALID_ARGUMENT;
+  if (R < 1) return LS_ERR_INVALID_ARGUMENT;
+  if (R >= (int64_t(1) << 31)) return LS_ERR_UNSUPPORTED;
+  if (workspace == nullptr || workspace_bytes < ls_replay_bwd_workspace_bytes(h, R))
+    return LS_ERR_WORKSPACE;
+  if (!aligned16(q) || !aligned16(k_suffix) || !aligned16(v_suffix) || !aligned16(o) ||
+      !aligned16(d_out) || !aligned16(dq) || !aligned16(dk_suffix) || !aligned16(dv_suffix) ||
+      !aligned16(workspace) || !aligned_n(lse, 4))
+    return LS_ERR_MISALIGNED;
+  uint32_t* status = nullptr;
+  st = enter(h, stream, &status);
+  if (st != LS_OK) return st;
+
+  BwdArgs a{};
+  a.sh = h->shape;
+  a.sh.R = R;
+  a.qt64 = 64 / a.sh.g;
+  a.tm_kp128 = &h->tm_k;
+  a.tm_vp128 = &h->tm_v;
+  a.tm_kp64 = &h->tm_k64;
+  a.tm_vp64 = &h->tm_v64;
+  const AttnShape& sh = a.sh;
+  st = encode_thd(&a.tm_q64, q, R, sh.Hq, sh.D, sh.g, a.qt64);
+  if (st == LS_OK) st = encode_thd(&a.tm_do64, d_out, R, sh.Hq, sh.D, sh.g, a.qt64);
+  if (st == LS_OK) st = encode_thd(&a.tm_q128, q, R, sh.Hq, sh.D, sh.g, sh.qt);
+  if (st == LS_OK) st = encode_thd(&a.tm_do128, d_out, R, sh.Hq, sh.D, sh.g, sh.qt);
+  if (st == LS_OK) st = encode_thd(&a.tm_ks128, k_suffix, R, sh.Hkv, sh.D, 1, 128);
+  if (st == LS_OK) st = encode_thd(&a.tm_vs128, v_suffix, R, sh.Hkv, sh.D, 1, 128);
+  if (st == LS_OK) st = encode_thd(&a.tm_ks64, k_suffix, R, sh.Hkv, sh.D, 1, 64);
+  if (st == LS_OK) st = encode_thd(&a.tm_vs64, v_suffix, R, sh.Hkv, sh.D, 1, 64);
+  if (st != LS_OK) return st;
+  float2* rowstats = static_cast<float2*>(workspace);
+  a.rowstats = rowstats;
+  a.dq = static_cast<uint16_t*>(dq);
+  a.dk_suf = static_cast<uint16_t*>(dk_suffix);
+  a.dv_suf = static_cast<uint16_t*>(dv_suffix);
+  a.dk_acc = h->dk_acc;
+  a.dv_acc = h->dv_acc;
+  a.status = status;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_bwd_prep(static_cast<const uint16_t*>(o),
+                                  static_cast<const uint16_t*>(d_out), lse, rowstats, sh, a.qt64, s);
+  if (e != cudaSuccess) return cuda_fail(e, "replay backward prep launch");
+  e = launch_attn_bwd_dkdv(a, s);
+  if (e != cudaSuccess) return cuda_fail(e, "replay backward dK/dV launch");
+  e = launch_attn_bwd_dq(a, s);
+  if (e != cudaSuccess) return cuda_fail(e, "replay backward dQ launch");
+  return LS_OK;
+}
+
+size_t ls_grpo_loss_workspace_bytes(int64_t R) {
+  if (R < 1) return 0;
+  return align_up(static_cast<size_t>(R) * sizeof(double), 256);
+}
+
+ls_status ls_grpo_loss(int64_t R, int64_t V, int32_t G, const void* logits, const int32_t* ids,
+                       const float* logp_old, double advantage, double eps, double* loss_accum,
+                       void* dlogits, uint8_t* clip_mask, float* logp_out, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  if (logits == nullptr || ids == nullptr || logp_old == nullptr || loss_accum == nullptr ||
+      dlogits == nullptr || clip_mask == nullptr)
+    return LS_ERR_INVALID_ARGUMENT;
+  if (R < 1 || V < 1 || G < 1) return LS_ERR_INVALID_ARGUMENT;
+  if (!std::isfinite(advantage) || !(eps >= 0.0 && eps < 1.0)) return LS_ERR_INVALID_ARGUMENT;
+  if (R >= (int64_t(1) << 31) || V >= (int64_t(1) << 31)) return LS_ERR_UNSUPPORTED;
+  if (workspace == nullptr || workspace_bytes < ls_grpo_loss_workspace_bytes(R))
+    return LS_ERR_WORKSPACE;
+  if (!aligned_n(logits, 2) || !aligned_n(dlogits, 2) || !aligned_n(ids, 4) ||
+      !aligned_n(logp_old, 4) || !aligned_n(loss_accum, 8) || !aligned16(workspace) ||
+      (logp_out != nullptr && !aligned_n(logp_out, 4)))
+    return LS_ERR_MISALIGNED;
+  uint32_t* status = nullptr;
+  ls_status st = enter(nullptr, stream, &status);
+  if (st != LS_OK) return st;
+  LossArgs a{};
+  a.R = R;
+  a.V = V;
+  a.G = G;
+  a.logits = static_cast<const uint16_t*>(logits);
+  a.ids = ids;
+  a.logp_old = logp_old;
+  a.A = advantage;
+  a.eps = eps;
+  a.loss_accum = loss_accum;
+  a.dlogits = static_cast<uint16_t*>(dlogits);
+  a.clip_mask = clip_mask;
+  a.logp_out = logp_out;
+  a.row_terms = static_cast<double*>(workspace);
+  a.status = status;
+  cudaError_t e = launch_grpo_loss(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? LS_OK : cuda_fail(e, "grpo loss launch");
+}
+
+ls_status ls_prefix_grad_finalize(ls_prefix_t h, float scale, void* dk_out, void* dv_out,
+                                  int out_is_fp32, int reset_acc, void* stream) {
+  ls_status st = check_handle(h);
+  if (st != LS_OK) return st;
+  if (!std::isfinite(scale)) return LS_ERR_INVALID_ARGUMENT;
+  if ((dk_out == nullptr) != (dv_out == nullptr)) return LS_ERR_INVALID_ARGUMENT;
+  const bool inplace = dk_out == nullptr;
+  if (inplace && reset_acc) return LS_ERR_INVALID_ARGUMENT;
+  if (!inplace && (!aligned16(dk_out) || !aligned16(dv_out))) return LS_ERR_MISALIGNED;
+  uint32_t* status = nullptr;
+  st = enter(h, stream, &status);
+  if (st != LS_OK) return st;
+  const size_t n = static_cast<size_t>(h->shape.P) * h->shape.Hkv * h->shape.D;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (inplace) {
+    e = launch_scale_inplace(h->dk_acc, n, scale, s);
+    if (e == cudaSuccess) e = launch_scale_inplace(h->dv_acc, n, scale, s);
+  } else {
+    e = launch_finalize(h->dk_acc, dk_out, n, scale, out_is_fp32 ? 1 : 0, reset_acc ? 1 : 0, s);
+    if (e == cudaSuccess)
+      e = launch_finalize(h->dv_acc, dv_out, n, scale, out_is_fp32 ? 1 : 0, reset_acc ? 1 : 0, s);
+  }
+  return e == cudaSuccess ? LS_OK : cuda_fail(e, "finalize launch");
+}
+
+ls_status ls_get_device_status(void* stream, uint32_t* bits) {
+  int dev = 0;
+  ls_status st = current_device(&dev);
+  if (st != LS_OK) return st;
+  uint32_t* sp = nullptr;
+  st = status_ptr(dev, &sp);
+  if (st != LS_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t host = 0, zero = 0;
+  cudaError_t e = cudaMemcpyAsync(&host, sp, sizeof(host), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(sp, &zero, sizeof(zero), cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "device status read");
+  if (bits != nullptr) *bits = host;
+  if (host & DEV_WAIT_TIMEOUT) return LS_ERR_TIMEOUT;
+  if (host != 0u) return LS_ERR_DEVICE_STATUS;
+  return LS_OK;
+}
+
+}  // extern "C"

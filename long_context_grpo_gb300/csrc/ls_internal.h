@@ -1,0 +1,83 @@
+// Internal launch interface between the C-ABI host layer (ls_api.cu) and the kernel
+// translation units.  Not installed; not part of the ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace ls {
+
+// ----- GRPO loss (k_loss.cu)
+struct LossArgs {
+  int64_t R, V;
+  int32_t G;
+  const uint16_t* logits;   // bf16 [R, V]
+  const int32_t* ids;       // [R]
+  const float* logp_old;    // [R]
+  double A, eps;
+  double* loss_accum;       // device scalar, +=
+  uint16_t* dlogits;        // bf16 [R, V]
+  uint8_t* clip_mask;       // [R]
+  float* logp_out;          // [R] or nullptr
+  double* row_terms;        // workspace [R]
+  uint32_t* status;
+};
+cudaError_t launch_grpo_loss(const LossArgs& a, cudaStream_t s);
+
+// ----- elementwise helpers (k_elementwise.cu)
+cudaError_t launch_zero_f32(float* p, size_t n, cudaStream_t s);
+cudaError_t launch_finalize(const float* acc, void* out, size_t n, float scale, int out_fp32,
+                            int reset, cudaStream_t s);
+cudaError_t launch_scale_inplace(float* acc, size_t n, float scale, cudaStream_t s);
+
+// ----- attention (k_attn_fwd.cu, k_attn_bwd.cu)
+struct AttnShape {
+  int64_t P, R;
+  int Hq, Hkv, D, g;
+  float scale;
+  int qt;        // queries per 128-row tile (= 128 / g)
+};
+
+struct FwdArgs {
+  AttnShape sh;
+  const CUtensorMap* tm_kp;   // prompt K [P][Hkv][D] 3-D map, box {64, 1, 128}
+  const CUtensorMap* tm_vp;
+  CUtensorMap tm_q;           // Q [R][Hq][D], box {64, g, qt}
+  CUtensorMap tm_ks, tm_vs;   // suffix K/V [R][Hkv][D], box {64, 1, 128}
+  uint16_t* o;
+  float* lse;
+  uint32_t* status;
+};
+cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t s);
+
+struct BwdArgs {
+  AttnShape sh;
+  int qt64;                       // queries per 64-row sub-tile (= 64 / g) used by dK/dV
+  const CUtensorMap* tm_kp128;    // prompt K/V, box {64, 1, 128} (dK/dV key tiles)
+  const CUtensorMap* tm_vp128;
+  const CUtensorMap* tm_kp64;     // prompt K/V, box {64, 1, 64} (dQ key steps)
+  const CUtensorMap* tm_vp64;
+  CUtensorMap tm_q64, tm_do64;    // [R][Hq][D], box {64, g, qt64}
+  CUtensorMap tm_q128, tm_do128;  // [R][Hq][D], box {64, g, qt}
+  CUtensorMap tm_ks128, tm_vs128; // suffix K/V, box {64, 1, 128}
+  CUtensorMap tm_ks64, tm_vs64;   // suffix K/V, box {64, 1, 64}
+  const float2* rowstats;         // [Hkv][n_q64][64] (LSE * log2 e, Delta), packed by sub-tile row
+  uint16_t* dq;                   // bf16 [R, Hq, D]
+  uint16_t* dk_suf;               // bf16 [R, Hkv, D]
+  uint16_t* dv_suf;
+  float* dk_acc;                  // fp32 [P, Hkv, D]
+  float* dv_acc;
+  uint32_t* status;
+};
+// rowstats[(kv, i, r)] for every 64-row sub-tile slot: valid rows get (LSE log2 e, Delta),
+// padding rows and rows past R get (+inf, 0) so their softmax probabilities are exactly 0.
+cudaError_t launch_bwd_prep(const uint16_t* o, const uint16_t* d_out, const float* lse,
+                            float2* rowstats, const AttnShape& sh, int qt64, cudaStream_t s);
+cudaError_t launch_attn_bwd_dkdv(const BwdArgs& a, cudaStream_t s);
+cudaError_t launch_attn_bwd_dq(const BwdArgs& a, cudaStream_t s);
+
+int num_sms();
+
+}  // namespace ls

@@ -49,6 +49,16 @@ def _f64(x):
     return np.asarray(x, dtype=np.float64)
 
 
+def _ids(ids):
+    try:
+        import torch
+        if isinstance(ids, torch.Tensor):
+            return ids.detach().to("cpu", torch.int64).numpy().reshape(-1)
+    except ImportError:  # pragma: no cover
+        pass
+    return np.asarray(ids).astype(np.int64).reshape(-1)
+
+
 def _lse_rows(X):
     m = X.max(axis=1, keepdims=True)
     return (m + np.log(np.exp(X - m).sum(axis=1, keepdims=True)))[:, 0]
@@ -57,7 +67,7 @@ def _lse_rows(X):
 def token_logp(logits, ids):
     """log softmax(x)_y per row, float64.  logits [R, V], ids [R]."""
     X = _f64(logits)
-    y = np.asarray(ids).astype(np.int64).reshape(-1)
+    y = _ids(ids)
     out = np.empty(X.shape[0])
     for r0 in range(0, X.shape[0], _ROW_CHUNK):
         r1 = min(X.shape[0], r0 + _ROW_CHUNK)
@@ -84,7 +94,7 @@ def grpo_loss(logits, ids, logp_old, A, eps, G, rows=None):
     selected rows' [n, V] when `rows` is given).  The loss always covers every token.
     """
     X = _f64(logits)
-    y = np.asarray(ids).astype(np.int64).reshape(-1)
+    y = _ids(ids)
     old = _f64(logp_old).reshape(-1)
     R, V = X.shape
     A = float(A)
