@@ -1,0 +1,458 @@
+"""Benchmark of the branch-replay hot path on GB300.
+
+One step = one GRPO group through the whole per-GPU hot path: prompt prepare (accumulator
+zeroing), then for each of the G responses serially the forward replay, the fused GRPO
+loss and the backward replay (prompt dK/dV accumulated in fp32), then the one prompt
+gradient finalization.  Inputs are synthetic and seeded, with the shapes and distributions
+of the workload table in long_context_grpo_gb300/workloads.py, resident in HBM before the
+timed region (they are far larger than L2, so no flush is needed between steps).
+
+Prints one JSON line.  `--impl reference` times the float64 CPU oracle instead, on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "branch-replay fwd+bwd TFLOP/s & response tok/s at P=2M; % of roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def pairs(P, R):
+    """Visible (query, key) pairs of one response per query head."""
+    return R * P + R * (R + 1) // 2
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index=0):
+        self.proc = None
+        self.sel = None
+        try:
+            import torch
+            props = torch.cuda.get_device_properties(device_index)
+            uuid = getattr(props, "uuid", None)
+            if uuid is not None:
+                self.sel = "GPU-%s" % uuid
+        except Exception:
+            self.sel = None
+
+    def start(self):
+        cmd = ["nvidia-smi", "--query-gpu=" + self.QUERY, "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.sel:
+            cmd += ["-i", self.sel]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------------------ CPU side
+def cpu_sample_inputs(w, seed, rows):
+    """Inputs of the bounded CPU sample: the full prompt of one kv head and the first `rows`
+    query rows of response 0 for one query head (same distributions as the workload)."""
+    from long_context_grpo_gb300 import workloads as wl
+    import dataclasses
+    w1 = dataclasses.replace(w, Hq=1, Hkv=1)
+    kp, vp = wl.prefix_kv(w1, seed, "cpu")
+    q, ks, vs, do = wl.response_attention(w1, 0, rows, seed, "cpu")
+    logits, ids, noise = wl.response_loss_inputs(w, 0, rows, seed, "cpu")
+    return kp, vp, q, ks, vs, do, logits, ids, noise
+
+
+def oracle_sample_step(w, inp, G):
+    """One bounded oracle step: fwd + bwd of `rows` query rows x 1 head against the full
+    prompt, plus the GRPO loss of those rows.  Returns algorithmic FLOPs of the sample."""
+    import oracle
+    kp, vp, q, ks, vs, do, logits, ids, noise = inp
+    rows = q.shape[0]
+    oracle.replay_response(kp, vp, q, ks, vs, do)
+    logp = oracle.token_logp(logits, ids)
+    oracle.grpo_loss(logits, ids, logp + noise.double().numpy(), 1.0, w.eps, G)
+    return 14 * w.D * pairs(w.P, rows)
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, w):
+    """The float64 oracle, as it stands, on the host cores: W warm-up + K timed steps of a
+    bounded sample of the workload."""
+    rows = args.cpu_rows
+    inp = cpu_sample_inputs(w, args.seed, rows)
+    for _ in range(args.warmup):
+        oracle_sample_step(w, inp, w.G)
+    t0 = time.perf_counter()
+    flops = 0
+    for _ in range(args.steps):
+        flops += oracle_sample_step(w, inp, w.G)
+    dt = time.perf_counter() - t0
+    tflops = flops / dt / 1e12
+    tok_s = args.steps * rows / w.Hq / dt
+    sample = ("float64 oracle: %d query rows x 1 of %d query heads of response 0 against the "
+              "full %d-token prompt (fwd + bwd), plus their GRPO loss over V=%d; "
+              "tok/s = rows / Hq per second" % (rows, w.Hq, w.P, w.V))
+    line = {"metric": METRIC, "value": tflops, "unit": "TFLOP/s", "impl": "reference",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "P": w.P, "G": w.G, "Hq": w.Hq, "Hkv": w.Hkv,
+                       "D": w.D, "V": w.V, "sample_rows": rows},
+            "response_tok_s": tok_s,
+            "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": cores(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+# ------------------------------------------------------------------------------ GPU side
+class Group:
+    """Device-resident inputs and reusable output buffers of one group."""
+
+    def __init__(self, w, seed, device):
+        import torch
+        import long_context_grpo_gb300 as ls
+        from long_context_grpo_gb300 import workloads as wl
+        self.w = w
+        self.R = wl.response_lengths(w, seed)
+        self.A = wl.group_advantages(wl.rewards(w, seed))
+        if all(a == 0.0 for a in self.A):      # degenerate draw: keep the loss path non-trivial
+            self.A = wl.group_advantages([float(i % 2) for i in range(w.G)])
+        self.kp, self.vp = wl.prefix_kv(w, seed, device)
+        self.resp = []
+        for i, Ri in enumerate(self.R):
+            q, ks, vs, do = wl.response_attention(w, i, Ri, seed, device)
+            logits, ids, noise = wl.response_loss_inputs(w, i, Ri, seed, device)
+            self.resp.append({"q": q, "ks": ks, "vs": vs, "do": do, "logits": logits,
+                              "ids": ids, "noise": noise, "old": None})
+        Rm = max(self.R)
+        f32, bf16 = torch.float32, torch.bfloat16
+        self.dk_acc = torch.empty(self.kp.shape, dtype=f32, device=device)
+        self.dv_acc = torch.empty(self.kp.shape, dtype=f32, device=device)
+        self.dk_out = torch.empty(self.kp.shape, dtype=bf16, device=device)
+        self.dv_out = torch.empty(self.kp.shape, dtype=bf16, device=device)
+        self.o = torch.empty((Rm, w.Hq, w.D), dtype=bf16, device=device)
+        self.lse = torch.empty((Rm, w.Hq), dtype=f32, device=device)
+        self.dq = torch.empty((Rm, w.Hq, w.D), dtype=bf16, device=device)
+        self.dks = torch.empty((Rm, w.Hkv, w.D), dtype=bf16, device=device)
+        self.dvs = torch.empty((Rm, w.Hkv, w.D), dtype=bf16, device=device)
+        self.dlog = torch.empty((Rm, w.V), dtype=bf16, device=device)
+        self.mask = torch.empty((Rm,), dtype=torch.uint8, device=device)
+        self.logp = torch.empty((Rm,), dtype=f32, device=device)
+        self.lws = torch.empty(ls.grpo_loss_workspace_bytes(Rm), dtype=torch.uint8, device=device)
+        pre = ls.Prefix(self.kp, self.vp, self.dk_acc, self.dv_acc, Hq=w.Hq)
+        self.bws = torch.empty(max(pre.bwd_workspace_bytes(Rm), 16), dtype=torch.uint8,
+                               device=device)
+        # old-policy log-probs: the current policy's token log-prob plus the drawn noise
+        scratch = torch.zeros(1, dtype=torch.float64, device=device)
+        for r, Ri in zip(self.resp, self.R):
+            zero_old = torch.zeros((Ri,), dtype=f32, device=device)
+            ls.grpo_loss(r["logits"], r["ids"], zero_old, 0.0, w.eps, w.G, scratch,
+                         dlogits=self.dlog[:Ri], clip_mask=self.mask[:Ri],
+                         logp_out=self.logp[:Ri], workspace=self.lws)
+            r["old"] = self.logp[:Ri] + r["noise"]
+        pre.close()
+        torch.cuda.synchronize()
+
+    def inputs(self):
+        out = [self.kp, self.vp]
+        for r in self.resp:
+            out += [r["q"], r["ks"], r["vs"], r["do"], r["logits"], r["ids"], r["old"]]
+        return out
+
+    def step(self, loss_slot):
+        import long_context_grpo_gb300 as ls
+        w = self.w
+        pre = ls.Prefix(self.kp, self.vp, self.dk_acc, self.dv_acc, Hq=w.Hq)
+        for i, (r, Ri) in enumerate(zip(self.resp, self.R)):
+            o, lse = pre.fwd(r["q"], r["ks"], r["vs"], o=self.o[:Ri], lse=self.lse[:Ri])
+            ls.grpo_loss(r["logits"], r["ids"], r["old"], self.A[i], w.eps, w.G, loss_slot,
+                         dlogits=self.dlog[:Ri], clip_mask=self.mask[:Ri],
+                         logp_out=self.logp[:Ri], workspace=self.lws)
+            pre.bwd(r["q"], r["ks"], r["vs"], o, lse, r["do"], dq=self.dq[:Ri],
+                    dk_suffix=self.dks[:Ri], dv_suffix=self.dvs[:Ri], workspace=self.bws)
+        pre.finalize(1.0, self.dk_out, self.dv_out)
+        pre.close()
+
+    def flops(self):
+        w = self.w
+        return sum(14 * w.D * w.Hq * pairs(w.P, Ri) for Ri in self.R)
+
+    def kernel_work(self):
+        """Algorithmic work per kernel id for one step: (amount, unit)."""
+        w = self.w
+        pr = sum(pairs(w.P, Ri) for Ri in self.R)
+        n = w.P * w.Hkv * w.D
+        return {
+            "replay_fwd": (4 * w.D * w.Hq * pr, "flop"),
+            "bwd_dkdv": (8 * w.D * w.Hq * pr, "flop"),
+            "bwd_dq": (2 * w.D * w.Hq * pr, "flop"),
+            "grpo_loss": (sum(Ri * (4 * w.V + 12) for Ri in self.R), "byte"),
+            "bwd_prep": (sum(Ri * w.Hq * (4 * w.D + 4) for Ri in self.R), "byte"),
+            "finalize": (2 * n * 6, "byte"),
+            "zero": (2 * n * 4, "byte"),
+        }
+
+
+def run_ours(args, w):
+    import torch
+    import long_context_grpo_gb300 as ls
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum_over_ranks(x):
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t)
+        return float(t.item())
+
+    grp = Group(w, args.seed + rank, dev)
+    losses = torch.zeros(args.warmup + 2 * args.steps + 2, dtype=torch.float64, device=dev)
+    slot = 0
+    for _ in range(args.warmup):
+        grp.step(losses[slot:slot + 1])
+        slot += 1
+    torch.cuda.synchronize()
+    st = ls.device_status()
+    if st != (0, 0):
+        raise RuntimeError("device status after warm-up: %s" % (st,))
+
+    # ---------------- device-resident timed region
+    stream = torch.cuda.current_stream()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev.index)
+    ls.timing_read()
+    ls.timing_enable(True)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        grp.step(losses[slot:slot + 1])
+        slot += 1
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ls.timing_enable(False)
+    kt = ls.timing_read()
+    barrier()
+    ms = ev0.elapsed_time(ev1)
+    ms_max = max_over_ranks(ms)
+    flops_all = sum_over_ranks(grp.flops() * args.steps)
+    toks_all = sum_over_ranks(sum(grp.R) * args.steps)
+    value = flops_all / (ms_max / 1e3) / 1e12
+    tok_s = toks_all / (ms_max / 1e3)
+    st = ls.device_status()
+    if st != (0, 0):
+        raise RuntimeError("device status after timed steps: %s" % (st,))
+
+    # ---------------- per-kernel roofline
+    peaks, peak_src = load_peaks()
+    work = grp.kernel_work()
+    kernels = {}
+    for name, (tot_ms, n) in kt.items():
+        if n == 0 or tot_ms <= 0:
+            continue
+        amount, unit = work[name]
+        per_launch_amount = amount * args.steps / n
+        avg_ms = tot_ms / n
+        if unit == "flop":
+            ach = per_launch_amount / (avg_ms / 1e3) / 1e12
+            pk, pu, bound = peaks["bf16_tflops_sustained"], "TFLOP/s", "tensor"
+        else:
+            ach = per_launch_amount / (avg_ms / 1e3) / 1e9
+            pk, pu, bound = peaks["hbm_gbs"], "GB/s", "hbm"
+        kernels[name] = {"launches": n, "avg_ms": avg_ms, "share": tot_ms / ms,
+                         "bound": bound, "achieved": ach, "peak": pk, "unit": pu,
+                         "frac": ach / pk}
+    dom = max(kernels, key=lambda k: kernels[k]["share"])
+    d = kernels[dom]
+    roofline = {"kernel": dom, "bound": d["bound"], "achieved": d["achieved"], "peak": d["peak"],
+                "unit": d["unit"], "frac": d["frac"], "traffic": None,
+                "peak_source": peak_src + (" sustained bf16" if d["bound"] == "tensor" else " HBM copy")}
+    launches = sum(v["launches"] for v in kernels.values())
+
+    # ---------------- end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        dev_in = grp.inputs()
+        host_in = []
+        for t in dev_in:
+            h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            h.copy_(t)
+            host_in.append(h)
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
+        host_loss = torch.empty(1, dtype=torch.float64).pin_memory()
+
+        def e2e_step():
+            for h, d_ in zip(host_in, dev_in):
+                d_.copy_(h, non_blocking=True)
+            grp.step(losses[slot:slot + 1])
+            host_loss.copy_(losses[slot:slot + 1], non_blocking=True)
+
+        e2e_step()   # untimed
+        torch.cuda.synchronize()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = max_over_ranks(e0.elapsed_time(e1))
+        e2e = {"value": flops_all / (ems / 1e3) / 1e12, "unit": "TFLOP/s",
+               "response_tok_s": toks_all / (ems / 1e3), "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": 8}
+        del host_in
+
+    # ---------------- CPU baseline (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rows = args.cpu_rows
+        inp = cpu_sample_inputs(w, args.seed, rows)
+        t0 = time.perf_counter()
+        fl = oracle_sample_step(w, inp, w.G)
+        dt = time.perf_counter() - t0
+        cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cores(), "kind": "oracle",
+               "sample": "float64 oracle, %d query rows x 1 of %d query heads of response 0 "
+                         "against the full %d-token prompt (fwd + bwd) plus their GRPO loss; "
+                         "%.1f s" % (rows, w.Hq, w.P, dt)}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": w.name, "P": w.P, "G": w.G,
+                           "R": grp.R if world == 1 else "per-rank draws",
+                           "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D, "V": w.V,
+                           "parallelism": "independent groups per GPU" if world > 1 else "1 GPU",
+                           "l2": "inputs larger than L2 (no flush)"},
+                "response_tok_s": tok_s,
+                "roofline": roofline,
+                "kernels": kernels,
+                "gpu_launches": launches,
+                "clocks": clk,
+                "e2e": e2e,
+                "cpu_baseline": cpu,
+                "receipt": {"gradient_semantics": "prompt dK/dV exposed (fp32, group-summed), "
+                                                  "not propagated",
+                            "residency": "prompt K/V resident in HBM for the group",
+                            "topology": "%d GPU(s), no collective" % world,
+                            "staleness": "none (prepared every step)"}}
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="p2m")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-rows", type=int, default=8)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("at least 3 warm-up steps")
+    from long_context_grpo_gb300 import workloads as wl
+    w = wl.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        if int(os.environ.get("RANK", "0")) != 0:
+            return
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

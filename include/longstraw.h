@@ -183,6 +183,28 @@ ls_status ls_prefix_grad_finalize(ls_prefix_t h, float scale, void* dk_out, void
  */
 ls_status ls_get_device_status(void* stream, uint32_t* bits);
 
+/*
+ * Kernel timing (tracing aid).  While enabled, the library brackets every kernel launch it
+ * makes with a pair of CUDA events recorded on the launch's own stream.  ls_timing_read
+ * synchronises those events and returns, per kernel id, the summed device time (ms) and
+ * the number of launches since the previous read, then forgets them.  Host-side state
+ * only; thread-compatible, not thread-safe.  Disabled by default (zero overhead).
+ */
+typedef enum {
+  LS_KERNEL_ZERO = 0,          /* accumulator zeroing (prepare)                   */
+  LS_KERNEL_REPLAY_FWD = 1,    /* forward replay                                  */
+  LS_KERNEL_BWD_PREP = 2,      /* Delta and row statistics                        */
+  LS_KERNEL_BWD_DKDV = 3,      /* dK/dV and prompt accumulation                   */
+  LS_KERNEL_BWD_DQ = 4,        /* dQ                                              */
+  LS_KERNEL_GRPO_LOSS = 5,     /* loss row pass + fixed-order reduction           */
+  LS_KERNEL_FINALIZE = 6,      /* prompt-gradient finalization                    */
+  LS_KERNEL_COUNT = 7
+} ls_kernel_id;
+
+ls_status ls_timing_enable(int enable);
+/* total_ms and launches have room for n >= LS_KERNEL_COUNT entries (host arrays). */
+ls_status ls_timing_read(double* total_ms, int64_t* launches, int n);
+
 const char* ls_status_string(ls_status s);
 
 /* Message of the last CUDA failure seen by this thread ("" if none). */

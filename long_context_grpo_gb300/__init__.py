@@ -7,7 +7,8 @@ it is missing.
 __version__ = "0.1.0"
 
 _BINDING = ("Prefix", "grpo_loss", "grpo_loss_workspace_bytes", "device_status",
-            "LongStrawError", "library_path", "STATUS_NAMES")
+            "LongStrawError", "library_path", "STATUS_NAMES", "timing_enable", "timing_read",
+            "KERNEL_NAMES")
 
 
 def __getattr__(name):

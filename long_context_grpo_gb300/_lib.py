@@ -58,6 +58,9 @@ def _load():
         "ls_prefix_grad_finalize": (ctypes.c_int, [vp, ctypes.c_float, vp, vp, ctypes.c_int,
                                                    ctypes.c_int, vp]),
         "ls_get_device_status": (ctypes.c_int, [vp, ctypes.POINTER(ctypes.c_uint32)]),
+        "ls_timing_enable": (ctypes.c_int, [ctypes.c_int]),
+        "ls_timing_read": (ctypes.c_int, [ctypes.POINTER(ctypes.c_double),
+                                          ctypes.POINTER(ctypes.c_int64), ctypes.c_int]),
         "ls_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "ls_last_error": (ctypes.c_char_p, []),
         "ls_version": (ctypes.c_char_p, []),
@@ -211,6 +214,22 @@ def grpo_loss(logits, ids, logp_old, advantage: float, eps: float, G: int, loss_
         _ptr(logp_out, "logp_out", torch.float32, (R,)),
         _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream()), "ls_grpo_loss")
     return dlogits, clip_mask, logp_out
+
+
+KERNEL_NAMES = ("zero", "replay_fwd", "bwd_prep", "bwd_dkdv", "bwd_dq", "grpo_loss", "finalize")
+
+
+def timing_enable(on: bool = True):
+    _check(_lib().ls_timing_enable(1 if on else 0), "ls_timing_enable")
+
+
+def timing_read():
+    """{kernel name: (total ms, launches)} since the previous read."""
+    n = len(KERNEL_NAMES)
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_int64 * n)()
+    _check(_lib().ls_timing_read(ms, cnt, n), "ls_timing_read")
+    return {KERNEL_NAMES[i]: (ms[i], cnt[i]) for i in range(n)}
 
 
 def device_status():

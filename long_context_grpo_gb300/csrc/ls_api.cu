@@ -11,6 +11,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <vector>
 
 #include "../../include/longstraw.h"
 #include "ls_internal.h"
@@ -109,6 +110,50 @@ ls_status encode_thd(CUtensorMap* m, const void* base, int64_t T, int H, int D, 
 }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ----- optional per-launch timing (ls_timing_enable / ls_timing_read)
+struct TimedLaunch {
+  int kernel;
+  cudaEvent_t start, stop;
+};
+std::mutex g_timing_mu;
+bool g_timing = false;
+std::vector<TimedLaunch> g_timed;
+std::vector<cudaEvent_t> g_free_events;
+
+cudaEvent_t take_event() {
+  if (!g_free_events.empty()) {
+    cudaEvent_t e = g_free_events.back();
+    g_free_events.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Brackets the launches made during its lifetime when timing is enabled.
+class LaunchTimer {
+ public:
+  LaunchTimer(int kernel, cudaStream_t s) : kernel_(kernel), s_(s) {
+    std::lock_guard<std::mutex> lk(g_timing_mu);
+    if (!g_timing) return;
+    start_ = take_event();
+    stop_ = take_event();
+    if (start_ && stop_) cudaEventRecord(start_, s_);
+  }
+  ~LaunchTimer() {
+    if (!start_ || !stop_) return;
+    cudaEventRecord(stop_, s_);
+    std::lock_guard<std::mutex> lk(g_timing_mu);
+    g_timed.push_back({kernel_, start_, stop_});
+  }
+
+ private:
+  int kernel_;
+  cudaStream_t s_;
+  cudaEvent_t start_ = nullptr, stop_ = nullptr;
+};
 
 }  // namespace
 
@@ -233,8 +278,12 @@ ls_status ls_prefix_prepare(const ls_prefix_desc* d, ls_prefix_t* out, void* str
   }
   const size_t n = static_cast<size_t>(d->P) * d->Hkv * d->D;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_zero_f32(d->dk_acc, n, s);
-  if (e == cudaSuccess) e = launch_zero_f32(d->dv_acc, n, s);
+  cudaError_t e;
+  {
+    LaunchTimer t(LS_KERNEL_ZERO, s);
+    e = launch_zero_f32(d->dk_acc, n, s);
+    if (e == cudaSuccess) e = launch_zero_f32(d->dv_acc, n, s);
+  }
   if (e != cudaSuccess) {
     delete h;
     return cuda_fail(e, "prefix accumulator zeroing");
@@ -281,7 +330,11 @@ ls_status ls_replay_fwd(ls_prefix_t h, int64_t R, const void* q, const void* k_s
   a.o = static_cast<uint16_t*>(o);
   a.lse = lse;
   a.status = status;
-  cudaError_t e = launch_attn_fwd(a, static_cast<cudaStream_t>(stream));
+  cudaError_t e;
+  {
+    LaunchTimer t(LS_KERNEL_REPLAY_FWD, static_cast<cudaStream_t>(stream));
+    e = launch_attn_fwd(a, static_cast<cudaStream_t>(stream));
+  }
   return e == cudaSuccess ? LS_OK : cuda_fail(e, "replay forward launch");
 }
 
@@ -341,12 +394,22 @@ ls_status ls_replay_bwd(ls_prefix_t h, int64_t R, const void* q, const void* k_s
   a.dv_acc = h->dv_acc;
   a.status = status;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_bwd_prep(static_cast<const uint16_t*>(o),
-                                  static_cast<const uint16_t*>(d_out), lse, rowstats, sh, a.qt64, s);
+  cudaError_t e;
+  {
+    LaunchTimer t(LS_KERNEL_BWD_PREP, s);
+    e = launch_bwd_prep(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(d_out), lse,
+                        rowstats, sh, a.qt64, s);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "replay backward prep launch");
-  e = launch_attn_bwd_dkdv(a, s);
+  {
+    LaunchTimer t(LS_KERNEL_BWD_DKDV, s);
+    e = launch_attn_bwd_dkdv(a, s);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "replay backward dK/dV launch");
-  e = launch_attn_bwd_dq(a, s);
+  {
+    LaunchTimer t(LS_KERNEL_BWD_DQ, s);
+    e = launch_attn_bwd_dq(a, s);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "replay backward dQ launch");
   return LS_OK;
 }
@@ -390,7 +453,11 @@ ls_status ls_grpo_loss(int64_t R, int64_t V, int32_t G, const void* logits, cons
   a.logp_out = logp_out;
   a.row_terms = static_cast<double*>(workspace);
   a.status = status;
-  cudaError_t e = launch_grpo_loss(a, static_cast<cudaStream_t>(stream));
+  cudaError_t e;
+  {
+    LaunchTimer t(LS_KERNEL_GRPO_LOSS, static_cast<cudaStream_t>(stream));
+    e = launch_grpo_loss(a, static_cast<cudaStream_t>(stream));
+  }
   return e == cudaSuccess ? LS_OK : cuda_fail(e, "grpo loss launch");
 }
 
@@ -409,6 +476,7 @@ ls_status ls_prefix_grad_finalize(ls_prefix_t h, float scale, void* dk_out, void
   const size_t n = static_cast<size_t>(h->shape.P) * h->shape.Hkv * h->shape.D;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
+  LaunchTimer t(LS_KERNEL_FINALIZE, s);
   if (inplace) {
     e = launch_scale_inplace(h->dk_acc, n, scale, s);
     if (e == cudaSuccess) e = launch_scale_inplace(h->dv_acc, n, scale, s);
@@ -418,6 +486,44 @@ ls_status ls_prefix_grad_finalize(ls_prefix_t h, float scale, void* dk_out, void
       e = launch_finalize(h->dv_acc, dv_out, n, scale, out_is_fp32 ? 1 : 0, reset_acc ? 1 : 0, s);
   }
   return e == cudaSuccess ? LS_OK : cuda_fail(e, "finalize launch");
+}
+
+ls_status ls_timing_enable(int enable) {
+  std::lock_guard<std::mutex> lk(g_timing_mu);
+  g_timing = enable != 0;
+  return LS_OK;
+}
+
+ls_status ls_timing_read(double* total_ms, int64_t* launches, int n) {
+  if (total_ms == nullptr || launches == nullptr || n < LS_KERNEL_COUNT)
+    return LS_ERR_INVALID_ARGUMENT;
+  for (int i = 0; i < n; ++i) {
+    total_ms[i] = 0.0;
+    launches[i] = 0;
+  }
+  std::vector<TimedLaunch> done;
+  {
+    std::lock_guard<std::mutex> lk(g_timing_mu);
+    done.swap(g_timed);
+  }
+  ls_status st = LS_OK;
+  for (const TimedLaunch& t : done) {
+    float ms = 0.0f;
+    cudaError_t e = cudaEventSynchronize(t.stop);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, t.start, t.stop);
+    if (e != cudaSuccess) {
+      st = cuda_fail(e, "timing event");
+    } else {
+      total_ms[t.kernel] += ms;
+      launches[t.kernel] += 1;
+    }
+  }
+  std::lock_guard<std::mutex> lk(g_timing_mu);
+  for (const TimedLaunch& t : done) {
+    g_free_events.push_back(t.start);
+    g_free_events.push_back(t.stop);
+  }
+  return st;
 }
 
 ls_status ls_get_device_status(void* stream, uint32_t* bits) {
