@@ -20,7 +20,9 @@
 //   removes every dQ atomic (the prompt dimension is ~170x the suffix at a 2M prompt).
 //
 // Both kernels: warp 0 = TMA producer, warp 1 = MMA issuer, warp 2 = TMEM owner,
-// warps 4-11 = two softmax warpgroups that alternate over the double-buffered TMEM tiles.
+// warps 4-11 = two softmax warpgroups.  Both warpgroups work on every double-buffered TMEM
+// tile, each on half of its columns, which halves the softmax latency on the MMA's
+// critical path (S/dP of step j -> dS of step j -> the accumulate MMA of step j).
 // Every wait is bounded (status word + clean exit on timeout).
 #include "ls_internal.h"
 #include "ptx.cuh"
@@ -136,7 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars[C::kBarSFull + b], 1);
-      mbar_init(&bars[C::kBarDSFull + b], 128);
+      mbar_init(&bars[C::kBarDSFull + b], 256);
     }
     mbar_init(&bars[C::kBarAccDone], 1);
     mbar_init(&bars[C::kBarAccFree], 256);
@@ -164,7 +166,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_do);
       uint32_t qit = 0, uc = 0;
-      uint32_t issued[C::kNS] = {};
       bool ok = true, kv_pending = false;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
         const KvUnit w = make_kv_unit(u, sh, qt64, n_q64);
@@ -194,13 +195,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           bulk_load(base + 2 * C::kSub, rowstats + (static_cast<int64_t>(w.kv) * n_q64 + i) * 64,
                     512, &bars[C::kBarQFull + st]);
-          ++issued[st];
         }
       }
       if (!ok) {
         *vabort = 1;
-        for (int s = 0; s < C::kNS; ++s)
-          if (issued[s]) mbar_wait_ns(&bars[C::kBarQFull + s], (issued[s] - 1) & 1u, 200000000ull);
+        // drain this thread's own copies still in flight (the last kNS issues)
+        for (uint32_t it = qit > static_cast<uint32_t>(C::kNS) ? qit - C::kNS : 0u; it < qit; ++it)
+          mbar_wait_ns(&bars[C::kBarQFull + it % C::kNS], (it / C::kNS) & 1u, 200000000ull);
         if (kv_pending) mbar_wait_ns(&bars[C::kBarKVFull], (uc) & 1u, 200000000ull);
       }
     }
@@ -210,28 +211,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdAcc = idesc_bf16(128, D, false, true);
       const uint32_t sK = smem_u32(smem + C::kOffK), sV = smem_u32(smem + C::kOffV);
       const uint32_t sStage = smem_u32(smem + C::kOffStage);
-      uint32_t qit = 0, uc = 0, dsph[2] = {0u, 0u};
+      uint32_t qit = 0, uc = 0, dsph = 0u;   // bit b: parity of the next wait on buffer b
       bool ok = true;
+      const uint64_t dK0 = smem_desc(sK, 16, 1024), dV0 = smem_desc(sV, 16, 1024);
+      const uint64_t dS0 = smem_desc(sStage, 16, 1024);         // K-major view of a stage
+      const uint64_t dM0 = smem_desc(sStage, 8192, 1024);       // MN-major view of a stage
       auto issue_s = [&](int b, uint32_t st) {
-        const uint32_t sQ = sStage + st * C::kStage, sdO = sQ + C::kSub;
+        const uint64_t q = dS0 + static_cast<uint64_t>((st * C::kStage) >> 4);
+        const uint64_t o = q + static_cast<uint64_t>(C::kSub >> 4);
+        const uint32_t ds = tmem + C::col_s(b), dp = tmem + C::col_dp(b);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t oa = (kk >> 2) * 16384 + (kk & 3) * 32;
-          const uint32_t ob = (kk >> 2) * 8192 + (kk & 3) * 32;
-          mma_bf16_ss(tmem + C::col_s(b), smem_desc(sK + oa, 16, 1024),
-                      smem_desc(sQ + ob, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
-          mma_bf16_ss(tmem + C::col_dp(b), smem_desc(sV + oa, 16, 1024),
-                      smem_desc(sdO + ob, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+          const uint64_t oa = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+          const uint64_t ob = static_cast<uint64_t>(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4);
+          mma_bf16_ss(ds, dK0 + oa, q + ob, kIdS, kk > 0 ? 1u : 0u);
+          mma_bf16_ss(dp, dV0 + oa, o + ob, kIdS, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_acc = [&](int b, uint32_t st, bool acc) {
-        const uint32_t sQ = sStage + st * C::kStage, sdO = sQ + C::kSub;
+        const uint64_t q = dM0 + static_cast<uint64_t>((st * C::kStage) >> 4);
+        const uint64_t o = q + static_cast<uint64_t>(C::kSub >> 4);
+        const uint32_t ps = tmem + C::col_s(b), pd = tmem + C::col_dp(b);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          mma_bf16_ts(tmem + C::kColDV, tmem + C::col_s(b) + kk * 8,
-                      smem_desc(sdO + kk * 2048, 8192, 1024), kIdAcc, (acc || kk > 0) ? 1u : 0u);
-          mma_bf16_ts(tmem + C::kColDK, tmem + C::col_dp(b) + kk * 8,
-                      smem_desc(sQ + kk * 2048, 8192, 1024), kIdAcc, (acc || kk > 0) ? 1u : 0u);
+          const uint64_t ok_ = static_cast<uint64_t>((kk * 2048) >> 4);
+          mma_bf16_ts(tmem + C::kColDV, ps + kk * 8, o + ok_, kIdAcc, (acc || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + C::kColDK, pd + kk * 8, q + ok_, kIdAcc, (acc || kk > 0) ? 1u : 0u);
         }
       };
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
@@ -251,9 +256,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int li = 0; li < w.n && ok; ++li) {
           const int b = li & 1;
           const uint32_t st = (qit + li) % C::kNS;
-          ok = mbar_wait(&bars[C::kBarDSFull + b], dsph[b], status, vabort);
+          ok = mbar_wait(&bars[C::kBarDSFull + b], (dsph >> b) & 1u, status, vabort);
           if (!ok) break;
-          dsph[b] ^= 1u;
+          dsph ^= 1u << b;
           if (li == 0 && uc > 0) {
             ok = mbar_wait(&bars[C::kBarAccFree], (uc - 1) & 1u, status, vabort);
             if (!ok) break;
@@ -286,56 +291,62 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = quarter * 32 + lane;   // key within the tile
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float c2 = sh.scale * kLog2e;
-    uint32_t sph = 0u, qit = 0u, uc = 0u;
+    uint32_t sph = 0u, qit = 0u, uc = 0u;   // bit b: parity of the next wait on buffer b
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
       const KvUnit w = make_kv_unit(u, sh, qt64, n_q64);
       const int key = w.key0 + row;
-      for (int li = wg; li < w.n; li += 2) {
+      // both warpgroups work on every sub-tile: warpgroup wg owns its rows [32 wg, 32 wg + 32)
+      for (int li = 0; li < w.n; ++li) {
+        const int b = li & 1;
         const uint32_t st = (qit + li) % C::kNS;
-        ok = mbar_wait(&bars[C::kBarSFull + wg], sph, status, vabort);
+        ok = mbar_wait(&bars[C::kBarSFull + b], (sph >> b) & 1u, status, vabort);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        sph ^= 1u;
+        sph ^= 1u << b;
         // acquire the row stats copied into this stage (long complete: the MMA waited on it)
         ok = mbar_wait(&bars[C::kBarQFull + st], ((qit + li) / C::kNS) & 1u, status, vabort);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        const float2* rs = reinterpret_cast<const float2*>(smem + C::kOffStage + st * C::kStage +
-                                                           2 * C::kSub);
+        const float4* rs4 = reinterpret_cast<const float4*>(smem + C::kOffStage + st * C::kStage +
+                                                            2 * C::kSub);
         // causal suffix: rows r < lo see only suffix keys < this key
         int lo = 0;
         if (!w.prompt) {
           const int v = sh.g * (key - (w.i0 + li) * qt64);
           lo = v < 0 ? 0 : (v > 64 ? 64 : v);
         }
+        uint32_t sv[32], dv[32];
+        tmem_ld32(lane_base + C::col_s(b) + wg * 32, sv);
+        tmem_ld32(lane_base + C::col_dp(b) + wg * 32, dv);
+        tmem_ld_wait();
+        float p[32];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t sv[32], dv[32];
-          tmem_ld32(lane_base + C::col_s(wg) + half * 32, sv);
-          tmem_ld32(lane_base + C::col_dp(wg) + half * 32, dv);
-          tmem_ld_wait();
-          uint32_t pw[16], dw[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int c = half * 32 + 2 * i;
-            const float2 s0 = rs[c], s1 = rs[c + 1];
-            float p0 = ex2_approx(fmaf(__uint_as_float(sv[2 * i]), c2, -s0.x));
-            float p1 = ex2_approx(fmaf(__uint_as_float(sv[2 * i + 1]), c2, -s1.x));
-            if (c < lo) p0 = 0.0f;
-            if (c + 1 < lo) p1 = 0.0f;
-            const float d0 = p0 * (__uint_as_float(dv[2 * i]) - s0.y);
-            const float d1 = p1 * (__uint_as_float(dv[2 * i + 1]) - s1.y);
-            pw[i] = pack_bf16x2(p0, p1);
-            dw[i] = pack_bf16x2(d0, d1);
-          }
-          tmem_st16(lane_base + C::col_s(wg) + half * 16, pw);
-          tmem_st16(lane_base + C::col_dp(wg) + half * 16, dw);
+        for (int i = 0; i < 16; ++i) {
+          const float4 st4 = rs4[wg * 16 + i];   // (LSE2, Delta) of rows c and c + 1
+          p[2 * i] = ex2_approx(fmaf(__uint_as_float(sv[2 * i]), c2, -st4.x));
+          p[2 * i + 1] = ex2_approx(fmaf(__uint_as_float(sv[2 * i + 1]), c2, -st4.z));
+          dv[2 * i] = __float_as_uint(__uint_as_float(dv[2 * i]) - st4.y);
+          dv[2 * i + 1] = __float_as_uint(__uint_as_float(dv[2 * i + 1]) - st4.w);
         }
+        if (lo > wg * 32) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (wg * 32 + i < lo) p[i] = 0.0f;
+        }
+        uint32_t pw[16], dw[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          pw[i] = pack_bf16x2(p[2 * i], p[2 * i + 1]);
+          dw[i] = pack_bf16x2(p[2 * i] * __uint_as_float(dv[2 * i]),
+                              p[2 * i + 1] * __uint_as_float(dv[2 * i + 1]));
+        }
+        tmem_st16(lane_base + C::col_s(b) + wg * 16, pw);
+        tmem_st16(lane_base + C::col_dp(b) + wg * 16, dw);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bars[C::kBarDSFull + wg]);
+        mbar_arrive(&bars[C::kBarDSFull + b]);
       }
       if (!ok) break;
       qit += w.n;
@@ -405,7 +416,7 @@ struct DqCfg {
   static constexpr int kStage = 2 * kKV;
   static constexpr int kOffQ = 0, kOffDO = kQ, kOffStage = 2 * kQ;
   static constexpr int kOffBar = kOffStage + kNS * kStage;
-  static constexpr int kBarQFull = 0, kBarQEmpty = 1, kBarKVFull = 2;
+  static constexpr int kBarQFull = 0, kBarQEmpty = 1, kBarQTmem = 2, kBarKVFull = 3;
   static constexpr int kBarKVEmpty = kBarKVFull + kNS;
   static constexpr int kBarSFull = kBarKVEmpty + kNS;
   static constexpr int kBarDSFull = kBarSFull + 2;
@@ -414,10 +425,14 @@ struct DqCfg {
   static constexpr int kBarDrain = kBarDQFree + 1;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kSmem = kOffBar + kNumBars * 8 + 16 + 1024;
-  // TMEM: S_b at 64 b (dS_b aliases its first 32 columns), dP_b at 128 + 64 b, dQ at 256.
+  // TMEM: S_b at 64 b (dS_b aliases its first 32 columns), dP_b at 128 + 64 b, dQ at 256,
+  // and the unit's Q and dO rows (bf16, the A operand of S = Q K^T and dP = dO V^T) at
+  // 384 and 384 + D/2, so those MMAs read only the 64-key K/V tile from shared memory.
   __host__ __device__ static constexpr uint32_t col_s(int b) { return 64u * b; }
   __host__ __device__ static constexpr uint32_t col_dp(int b) { return 128u + 64u * b; }
   static constexpr uint32_t kColDQ = 256u;
+  static constexpr uint32_t kColQ = 384u;
+  static constexpr uint32_t kColDO = 384u + D / 2;
 };
 
 struct QUnit {
@@ -465,14 +480,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(&bars[C::kBarQFull], 1);
-    mbar_init(&bars[C::kBarQEmpty], 1);
+    mbar_init(&bars[C::kBarQEmpty], 256);
+    mbar_init(&bars[C::kBarQTmem], 256);
     for (int i = 0; i < C::kNS; ++i) {
       mbar_init(&bars[C::kBarKVFull + i], 1);
       mbar_init(&bars[C::kBarKVEmpty + i], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars[C::kBarSFull + b], 1);
-      mbar_init(&bars[C::kBarDSFull + b], 128);
+      mbar_init(&bars[C::kBarDSFull + b], 256);
     }
     mbar_init(&bars[C::kBarDQDone], 1);
     mbar_init(&bars[C::kBarDQFree], 256);
@@ -499,7 +515,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_do);
       uint32_t kit = 0, uc = 0;
-      uint32_t issued[C::kNS] = {};
       bool ok = true;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
         const QUnit w = make_q_unit(u, sh, n_qt);
@@ -528,13 +543,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(base + C::kKV + b * 8192, pre ? &tm_vp : &tm_vs,
                         &bars[C::kBarKVFull + st], 64 * b, w.kv, key0);
           }
-          ++issued[st];
         }
       }
       if (!ok) {
         *vabort = 1;
-        for (int s = 0; s < C::kNS; ++s)
-          if (issued[s]) mbar_wait_ns(&bars[C::kBarKVFull + s], (issued[s] - 1) & 1u, 200000000ull);
+        for (uint32_t it = kit > static_cast<uint32_t>(C::kNS) ? kit - C::kNS : 0u; it < kit; ++it)
+          mbar_wait_ns(&bars[C::kBarKVFull + it % C::kNS], (it / C::kNS) & 1u, 200000000ull);
         mbar_wait_ns(&bars[C::kBarQFull], (uc) & 1u, 200000000ull);
       }
     }
@@ -542,32 +556,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(128, 64, false, false);
       constexpr uint32_t kIdQ = idesc_bf16(128, D, false, true);
-      const uint32_t sQ = smem_u32(smem + C::kOffQ), sdO = smem_u32(smem + C::kOffDO);
       const uint32_t sStage = smem_u32(smem + C::kOffStage);
-      uint32_t kit = 0, uc = 0, dsph[2] = {0u, 0u};
+      const uint64_t dK0 = smem_desc(sStage, 16, 1024);     // K-major view of a stage
+      const uint64_t dM0 = smem_desc(sStage, 8192, 1024);   // MN-major view of a stage
+      uint32_t kit = 0, uc = 0, dsph = 0u;   // bit b: parity of the next wait on buffer b
       bool ok = true;
       auto issue_s = [&](int b, uint32_t st) {
-        const uint32_t sK = sStage + st * C::kStage, sV = sK + C::kKV;
+        const uint64_t k = dK0 + static_cast<uint64_t>((st * C::kStage) >> 4);
+        const uint64_t v = k + static_cast<uint64_t>(C::kKV >> 4);
+        const uint32_t ds = tmem + C::col_s(b), dp = tmem + C::col_dp(b);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t oa = (kk >> 2) * 16384 + (kk & 3) * 32;
-          const uint32_t ob = (kk >> 2) * 8192 + (kk & 3) * 32;
-          mma_bf16_ss(tmem + C::col_s(b), smem_desc(sQ + oa, 16, 1024),
-                      smem_desc(sK + ob, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
-          mma_bf16_ss(tmem + C::col_dp(b), smem_desc(sdO + oa, 16, 1024),
-                      smem_desc(sV + ob, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+          const uint64_t ob = static_cast<uint64_t>(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4);
+          mma_bf16_ts(ds, tmem + C::kColQ + kk * 8, k + ob, kIdS, kk > 0 ? 1u : 0u);
+          mma_bf16_ts(dp, tmem + C::kColDO + kk * 8, v + ob, kIdS, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_dq = [&](int b, uint32_t st, bool acc) {
-        const uint32_t sK = sStage + st * C::kStage;
+        const uint64_t k = dM0 + static_cast<uint64_t>((st * C::kStage) >> 4);
+        const uint32_t a = tmem + C::col_s(b);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_bf16_ts(tmem + C::kColDQ, tmem + C::col_s(b) + kk * 8,
-                      smem_desc(sK + kk * 2048, 8192, 1024), kIdQ, (acc || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + C::kColDQ, a + kk * 8, k + static_cast<uint64_t>((kk * 2048) >> 4),
+                      kIdQ, (acc || kk > 0) ? 1u : 0u);
       };
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
         const QUnit w = make_q_unit(u, sh, n_qt);
-        ok = mbar_wait(&bars[C::kBarQFull], uc & 1u, status, vabort);
+        ok = mbar_wait(&bars[C::kBarQTmem], uc & 1u, status, vabort);
         if (!ok) break;
         tc_fence_after();
         const int npro = w.n < 2 ? w.n : 2;
@@ -582,9 +597,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < w.n && ok; ++j) {
           const int b = j & 1;
           const uint32_t st = (kit + j) % C::kNS;
-          ok = mbar_wait(&bars[C::kBarDSFull + b], dsph[b], status, vabort);
+          ok = mbar_wait(&bars[C::kBarDSFull + b], (dsph >> b) & 1u, status, vabort);
           if (!ok) break;
-          dsph[b] ^= 1u;
+          dsph ^= 1u << b;
           if (j == 0 && uc > 0) {
             ok = mbar_wait(&bars[C::kBarDQFree], (uc - 1) & 1u, status, vabort);
             if (!ok) break;
@@ -605,7 +620,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         kit += w.n;
         mma_commit(&bars[C::kBarDQDone]);
-        if (u + static_cast<int>(gridDim.x) < n_units) mma_commit(&bars[C::kBarQEmpty]);
       }
       if (!ok) *vabort = 1;
       mma_commit(&bars[C::kBarDrain]);
@@ -617,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float c2 = sh.scale * kLog2e;
-    uint32_t sph = 0u, uc = 0u;
+    uint32_t sph = 0u, uc = 0u;   // bit b: parity of the next wait on buffer b
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
       const QUnit w = make_q_unit(u, sh, n_qt);
@@ -630,11 +644,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r64 = (t - i64 * qt64) * sh.g + hg;
         st2 = rowstats[(static_cast<int64_t>(w.kv) * n_q64 + i64) * 64 + r64];
       }
-      for (int j = wg; j < w.n; j += 2) {
-        ok = mbar_wait(&bars[C::kBarSFull + wg], sph, status, vabort);
+      // stage this unit's Q (warpgroup 0) or dO (warpgroup 1) row into TMEM; the previous
+      // unit's MMAs have all completed (its dQ-done barrier was waited on)
+      ok = mbar_wait(&bars[C::kBarQFull], uc & 1u, status, vabort);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      {
+        const uint8_t* src = smem + (wg == 0 ? C::kOffQ : C::kOffDO);
+        const uint32_t col = wg == 0 ? C::kColQ : C::kColDO;
+#pragma unroll
+        for (int bx = 0; bx < C::kBoxes; ++bx) {
+          uint32_t v32[32];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 v = *reinterpret_cast<const uint4*>(src + bx * 16384 + sw128_offset(row, c));
+            v32[4 * c + 0] = v.x;
+            v32[4 * c + 1] = v.y;
+            v32[4 * c + 2] = v.z;
+            v32[4 * c + 3] = v.w;
+          }
+          tmem_st32(lane_base + col + bx * 32, v32);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars[C::kBarQTmem]);
+        mbar_arrive(&bars[C::kBarQEmpty]);
+      }
+      // both warpgroups work on every step: warpgroup wg owns key columns [32 wg, 32 wg + 32)
+      for (int j = 0; j < w.n; ++j) {
+        const int b = j & 1;
+        ok = mbar_wait(&bars[C::kBarSFull + b], (sph >> b) & 1u, status, vabort);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        sph ^= 1u;
+        sph ^= 1u << b;
         tc_fence_after();
         int lim = 64;
         if (j < w.n_pt) {
@@ -644,28 +686,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int v = t - 64 * (j - w.n_pt) + 1;
           lim = v < 0 ? 0 : (v > 64 ? 64 : v);
         }
+        uint32_t sv[32], dv[32];
+        tmem_ld32(lane_base + C::col_s(b) + wg * 32, sv);
+        tmem_ld32(lane_base + C::col_dp(b) + wg * 32, dv);
+        tmem_ld_wait();
+        float p[32];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t sv[32], dv[32];
-          tmem_ld32(lane_base + C::col_s(wg) + half * 32, sv);
-          tmem_ld32(lane_base + C::col_dp(wg) + half * 32, dv);
-          tmem_ld_wait();
-          uint32_t dw[16];
+        for (int i = 0; i < 32; ++i)
+          p[i] = ex2_approx(fmaf(__uint_as_float(sv[i]), c2, -st2.x));
+        if (lim < wg * 32 + 32) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int c = half * 32 + 2 * i;
-            float p0 = ex2_approx(fmaf(__uint_as_float(sv[2 * i]), c2, -st2.x));
-            float p1 = ex2_approx(fmaf(__uint_as_float(sv[2 * i + 1]), c2, -st2.x));
-            if (c >= lim) p0 = 0.0f;
-            if (c + 1 >= lim) p1 = 0.0f;
-            dw[i] = pack_bf16x2(p0 * (__uint_as_float(dv[2 * i]) - st2.y),
-                                p1 * (__uint_as_float(dv[2 * i + 1]) - st2.y));
-          }
-          tmem_st16(lane_base + C::col_s(wg) + half * 16, dw);
+          for (int i = 0; i < 32; ++i)
+            if (wg * 32 + i >= lim) p[i] = 0.0f;
         }
+        uint32_t dw[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          dw[i] = pack_bf16x2(p[2 * i] * (__uint_as_float(dv[2 * i]) - st2.y),
+                              p[2 * i + 1] * (__uint_as_float(dv[2 * i + 1]) - st2.y));
+        tmem_st16(lane_base + C::col_s(b) + wg * 16, dw);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bars[C::kBarDSFull + wg]);
+        mbar_arrive(&bars[C::kBarDSFull + b]);
       }
       if (!ok) break;
       // epilogue: dQ * s -> bf16; warpgroup 0 stores columns [0, D/2), warpgroup 1 the rest

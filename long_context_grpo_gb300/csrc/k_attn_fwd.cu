@@ -144,8 +144,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_ks);
       tma_prefetch_desc(&tm_vs);
       uint32_t kit = 0, vit = 0, uc = 0;
-      uint32_t k_issued[C::kNK > 0 ? C::kNK : 1] = {};
-      uint32_t v_issued[C::kNV > 0 ? C::kNV : 1] = {};
       bool ok = true;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
         const Unit w = make_unit(u, sh, n_pairs);
@@ -170,7 +168,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int b = 0; b < C::kBoxes; ++b)
               tma_load_3d(smem + C::kOffK + s * C::kTile + b * 16384, pre ? &tm_kp : &tm_ks,
                           &bars[C::kBarKFull + s], 64 * b, w.kv, key0);
-            ++k_issued[s];
             ++kit;
           }
           {
@@ -182,7 +179,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int b = 0; b < C::kBoxes; ++b)
               tma_load_3d(smem + C::kOffV + s * C::kTile + b * 16384, pre ? &tm_vp : &tm_vs,
                           &bars[C::kBarVFull + s], 64 * b, w.kv, key0);
-            ++v_issued[s];
             ++vit;
           }
         }
@@ -190,10 +186,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) {
         *vabort = 1;
         // drain this thread's own copies still in flight before the CTA may exit
-        for (int s = 0; s < C::kNK; ++s)
-          if (k_issued[s]) mbar_wait_ns(&bars[C::kBarKFull + s], (k_issued[s] - 1) & 1u, 200000000ull);
-        for (int s = 0; s < C::kNV; ++s)
-          if (v_issued[s]) mbar_wait_ns(&bars[C::kBarVFull + s], (v_issued[s] - 1) & 1u, 200000000ull);
+        for (uint32_t it = kit > static_cast<uint32_t>(C::kNK) ? kit - C::kNK : 0u; it < kit; ++it)
+          mbar_wait_ns(&bars[C::kBarKFull + it % C::kNK], (it / C::kNK) & 1u, 200000000ull);
+        for (uint32_t it = vit > static_cast<uint32_t>(C::kNV) ? vit - C::kNV : 0u; it < vit; ++it)
+          mbar_wait_ns(&bars[C::kBarVFull + it % C::kNV], (it / C::kNV) & 1u, 200000000ull);
         mbar_wait_ns(&bars[C::kBarQFull], (uc) & 1u, 200000000ull);
       }
     }
@@ -206,26 +202,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sK = smem_u32(smem + C::kOffK);
       const uint32_t sV = smem_u32(smem + C::kOffV);
       uint32_t kit = 0, vit = 0, uc = 0;
-      uint32_t pph[2] = {0u, 0u};    // p_full phase per tile
-      uint32_t uq[2] = {0u, 0u};     // units processed per tile
+      uint32_t pph = 0u;             // bit q: parity of the next p_full wait of tile q
+      uint32_t uq0 = 0u, uq1 = 0u;   // units processed per tile
       bool ok = true;
 
+      // Base descriptors; a tile or k-step offset is added to the start-address field
+      // (bits 0-13, address >> 4), which cannot carry out for shared addresses < 256 KB.
+      const uint64_t dQ0 = smem_desc(sQ, 16, 1024);
+      const uint64_t dK0 = smem_desc(sK, 16, 1024);
+      const uint64_t dV0 = smem_desc(sV, 16384, 1024);
       auto issue_s = [&](int q, uint32_t kstage) {
-        const uint32_t qa = sQ + q * C::kTile;
-        const uint32_t ka = sK + kstage * C::kTile;
+        const uint64_t qa = dQ0 + static_cast<uint64_t>((q * C::kTile) >> 4);
+        const uint64_t ka = dK0 + static_cast<uint64_t>((kstage * C::kTile) >> 4);
+        const uint32_t d = tmem + C::col_s(q);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_bf16_ss(tmem + C::col_s(q), smem_desc(qa + off, 16, 1024),
-                      smem_desc(ka + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+          const uint64_t off = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+          mma_bf16_ss(d, qa + off, ka + off, kIdS, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int q, uint32_t vstage, bool acc) {
-        const uint32_t va = sV + vstage * C::kTile;
+        const uint64_t va = dV0 + static_cast<uint64_t>((vstage * C::kTile) >> 4);
+        const uint32_t d = tmem + C::col_o(q), a = tmem + C::col_s(q);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ts(tmem + C::col_o(q), tmem + C::col_s(q) + kk * 8,
-                      smem_desc(va + kk * 2048, 16384, 1024), kIdPV, (acc || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(d, a + kk * 8, va + static_cast<uint64_t>((kk * 2048) >> 4), kIdPV,
+                      (acc || kk > 0) ? 1u : 0u);
       };
 
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
@@ -252,11 +254,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool more = (j + 1) < w.n_kt;
           uint32_t ks_next = kit % C::kNK;
           for (int q = 0; q < nq && ok; ++q) {
-            ok = mbar_wait(&bars[C::kBarPFull + q], pph[q], status, vabort);
+            ok = mbar_wait(&bars[C::kBarPFull + q], (pph >> q) & 1u, status, vabort);
             if (!ok) break;
-            pph[q] ^= 1u;
-            if (j == 0 && uq[q] > 0) {
-              ok = mbar_wait(&bars[C::kBarOFree + q], (uq[q] - 1) & 1u, status, vabort);
+            pph ^= 1u << q;
+            const uint32_t uqq = q ? uq1 : uq0;
+            if (j == 0 && uqq > 0) {
+              ok = mbar_wait(&bars[C::kBarOFree + q], (uqq - 1) & 1u, status, vabort);
               if (!ok) break;
             }
             tc_fence_after();
@@ -281,7 +284,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++vit;
         }
         if (!ok) break;
-        for (int q = 0; q < nq; ++q) ++uq[q];
+        ++uq0;
+        if (nq > 1) ++uq1;
         if (u + static_cast<int>(gridDim.x) < n_units) mma_commit(&bars[C::kBarQEmpty]);
       }
       if (!ok) *vabort = 1;
