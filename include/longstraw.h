@@ -165,6 +165,33 @@ ls_status ls_grpo_loss(int64_t R, int64_t V, int32_t G, const void* logits, cons
                        size_t workspace_bytes, void* stream);
 
 /*
+ * ls_grpo_loss_noalloc -- ls_grpo_loss for callers that cannot allocate device memory.
+ * (The reviewed pages have no counterpart: this is a deployment variant of the loss.)
+ * Same arguments, semantics and outputs as ls_grpo_loss, without the workspace: the
+ * per-row loss terms live in a fixed scratch array compiled into the library
+ * (ls_grpo_loss_noalloc_max_rows() rows of fp64, 512 KB, held by every GPU that loads the
+ * library until the process exits).  It is meant for callers that must not call
+ * cudaMalloc, e.g. code inside a fixed memory plan or an allocator-free host runtime that
+ * only passes pointers to buffers it already owns; it makes no cudaMalloc, cudaFree or other
+ * allocating call.
+ *   R > ls_grpo_loss_noalloc_max_rows() returns LS_ERR_UNSUPPORTED (message in
+ *   ls_last_error()) before anything is enqueued.
+ *   The first call on a device looks up the scratch array's device address (once, with
+ *   that device current); make that first call before any stream capture.
+ *   All calls on a device share the scratch: calls whose kernels may overlap on the GPU
+ *   (unordered streams or threads) race; calls ordered on one stream are safe.  Every
+ *   scratch entry a call reads was written earlier in the same call, so no clearing is
+ *   needed between calls.
+ */
+ls_status ls_grpo_loss_noalloc(int64_t R, int64_t V, int32_t G, const void* logits,
+                               const int32_t* ids, const float* logp_old, double advantage,
+                               double eps, double* loss_accum, void* dlogits,
+                               uint8_t* clip_mask, float* logp_out, void* stream);
+
+/* Largest R that ls_grpo_loss_noalloc accepts (its fixed scratch capacity in rows). */
+int64_t ls_grpo_loss_noalloc_max_rows(void);
+
+/*
  * ls_prefix_grad_finalize -- the group's one finalization (review section 2-1 step 5;
  * section 3-2 (7)).  out = scale * acc for the prompt dK and dV accumulators.
  *   dk_out, dv_out  device [P, Hkv, D], bf16 (out_is_fp32 = 0) or fp32 (out_is_fp32 = 1);

@@ -55,6 +55,9 @@ def _load():
         "ls_grpo_loss_workspace_bytes": (sz, [i64]),
         "ls_grpo_loss": (ctypes.c_int, [i64, i64, i32, vp, vp, vp, ctypes.c_double,
                                         ctypes.c_double, vp, vp, vp, vp, vp, sz, vp]),
+        "ls_grpo_loss_noalloc": (ctypes.c_int, [i64, i64, i32, vp, vp, vp, ctypes.c_double,
+                                                ctypes.c_double, vp, vp, vp, vp, vp]),
+        "ls_grpo_loss_noalloc_max_rows": (i64, []),
         "ls_prefix_grad_finalize": (ctypes.c_int, [vp, ctypes.c_float, vp, vp, ctypes.c_int,
                                                    ctypes.c_int, vp]),
         "ls_get_device_status": (ctypes.c_int, [vp, ctypes.POINTER(ctypes.c_uint32)]),

@@ -19,7 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "liblongstraw.so")
 
-SOURCES = ["ls_api.cu", "k_loss.cu", "k_elementwise.cu", "k_attn_fwd.cu", "k_attn_bwd.cu"]
+SOURCES = ["ls_api.cu", "k_loss.cu", "k_elementwise.cu", "k_attn_fwd.cu", "k_attn_bwd.cu",
+           "ls_noalloc.cu"]
 HEADERS = ["ls_internal.h", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE]

@@ -170,6 +170,16 @@ int num_sms() {
   return g_num_sms[dev];
 }
 
+// Accessors for other translation units of the library (no change to any entry point).
+int device_status_word(uint32_t** out) {
+  int dev = 0;
+  ls_status st = current_device(&dev);
+  if (st != LS_OK) return st;
+  return status_ptr(dev, out);
+}
+
+void set_last_error(const char* msg) { snprintf(t_last_error, sizeof(t_last_error), "%s", msg); }
+
 }  // namespace ls
 
 struct ls_prefix_s {

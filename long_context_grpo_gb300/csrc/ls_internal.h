@@ -79,5 +79,9 @@ cudaError_t launch_attn_bwd_dkdv(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_attn_bwd_dq(const BwdArgs& a, cudaStream_t s);
 
 int num_sms();
+// Status word of the current device (returns an ls_status value) and the per-thread
+// message behind ls_last_error(); both live in ls_api.cu.
+int device_status_word(uint32_t** out);
+void set_last_error(const char* msg);
 
 }  // namespace ls
