@@ -54,8 +54,8 @@ struct DkdvCfg {
   static constexpr int kBarDrain = kBarAccFree + 1;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kSmem = kOffBar + kNumBars * 8 + 16 + 1024;
-  // TMEM: S^T_b at 64 b, dP^T_b at 128 + 64 b (P^T / dS^T alias their first 32 columns),
-  // dV at 256, dK at 256 + D.
+  // TMEM: S^T_b at 64 b, dP^T_b at 128 + 64 b, dV at 256, dK at 256 + D.  Packed bf16
+  // P^T / dS^T of rows [32 w, 32 w + 32) alias columns [32 w, 32 w + 16) of S^T_b / dP^T_b.
   __host__ __device__ static constexpr uint32_t col_s(int b) { return 64u * b; }
   __host__ __device__ static constexpr uint32_t col_dp(int b) { return 128u + 64u * b; }
   static constexpr uint32_t kColDV = 256u;
@@ -234,9 +234,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ps = tmem + C::col_s(b), pd = tmem + C::col_dp(b);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
+          // rows 16 kk .. 16 kk + 15: packed by warpgroup kk / 2 at column 32 (kk / 2)
+          const uint32_t ac = 32u * (kk >> 1) + 8u * (kk & 1);
           const uint64_t ok_ = static_cast<uint64_t>((kk * 2048) >> 4);
-          mma_bf16_ts(tmem + C::kColDV, ps + kk * 8, o + ok_, kIdAcc, (acc || kk > 0) ? 1u : 0u);
-          mma_bf16_ts(tmem + C::kColDK, pd + kk * 8, q + ok_, kIdAcc, (acc || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + C::kColDV, ps + ac, o + ok_, kIdAcc, (acc || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + C::kColDK, pd + ac, q + ok_, kIdAcc, (acc || kk > 0) ? 1u : 0u);
         }
       };
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
@@ -342,8 +344,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           dw[i] = pack_bf16x2(p[2 * i] * __uint_as_float(dv[2 * i]),
                               p[2 * i + 1] * __uint_as_float(dv[2 * i + 1]));
         }
-        tmem_st16(lane_base + C::col_s(b) + wg * 16, pw);
-        tmem_st16(lane_base + C::col_dp(b) + wg * 16, dw);
+        // packed P^T / dS^T go to the first 16 of this warpgroup's own 32 columns, so no
+        // write can land on fp32 columns the other warpgroup has yet to read
+        tmem_st16(lane_base + C::col_s(b) + wg * 32, pw);
+        tmem_st16(lane_base + C::col_dp(b) + wg * 32, dw);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars[C::kBarDSFull + b]);
@@ -425,7 +429,8 @@ struct DqCfg {
   static constexpr int kBarDrain = kBarDQFree + 1;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kSmem = kOffBar + kNumBars * 8 + 16 + 1024;
-  // TMEM: S_b at 64 b (dS_b aliases its first 32 columns), dP_b at 128 + 64 b, dQ at 256,
+  // TMEM: S_b at 64 b (packed dS of keys [32 w, 32 w + 32) aliases its columns
+  // [32 w, 32 w + 16)), dP_b at 128 + 64 b, dQ at 256,
   // and the unit's Q and dO rows (bf16, the A operand of S = Q K^T and dP = dO V^T) at
   // 384 and 384 + D/2, so those MMAs read only the 64-key K/V tile from shared memory.
   __host__ __device__ static constexpr uint32_t col_s(int b) { return 64u * b; }
@@ -576,9 +581,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t k = dM0 + static_cast<uint64_t>((st * C::kStage) >> 4);
         const uint32_t a = tmem + C::col_s(b);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_bf16_ts(tmem + C::kColDQ, a + kk * 8, k + static_cast<uint64_t>((kk * 2048) >> 4),
-                      kIdQ, (acc || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 4; ++kk)   // keys 16 kk ..: packed by warpgroup kk / 2 at column 32 (kk / 2)
+          mma_bf16_ts(tmem + C::kColDQ, a + 32u * (kk >> 1) + 8u * (kk & 1),
+                      k + static_cast<uint64_t>((kk * 2048) >> 4), kIdQ, (acc || kk > 0) ? 1u : 0u);
       };
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
         const QUnit w = make_q_unit(u, sh, n_qt);
@@ -704,7 +709,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 16; ++i)
           dw[i] = pack_bf16x2(p[2 * i] * (__uint_as_float(dv[2 * i]) - st2.y),
                               p[2 * i + 1] * (__uint_as_float(dv[2 * i + 1]) - st2.y));
-        tmem_st16(lane_base + C::col_s(b) + wg * 16, dw);
+        // packed dS goes to the first 16 of this warpgroup's own 32 columns (no write lands
+        // on fp32 columns the other warpgroup has yet to read)
+        tmem_st16(lane_base + C::col_s(b) + wg * 32, dw);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars[C::kBarDSFull + b]);

@@ -59,7 +59,7 @@ def _kv_of(h: int, Hq: int, Hkv: int) -> int:
 
 
 def replay_response(k_prefix, v_prefix, q, k_suffix, v_suffix, d_out, scale=None,
-                    heads=None, want_grads=True):
+                    heads=None, want_grads=True, row_range=None):
     """Forward and backward of one response replayed against the prompt.
 
     Shapes: k_prefix, v_prefix [P, Hkv, D]; q, d_out [R, Hq, D]; k_suffix, v_suffix
@@ -89,8 +89,9 @@ def replay_response(k_prefix, v_prefix, q, k_suffix, v_suffix, d_out, scale=None
         kv = _kv_of(h, Hq, Hkv)
         K = np.concatenate([Kp[:, kv, :], Ks[:, kv, :]], axis=0)   # keys of X_i
         Vv = np.concatenate([Vp[:, kv, :], Vs[:, kv, :]], axis=0)
-        for t0 in range(0, R, _ROW_CHUNK):
-            t1 = min(R, t0 + _ROW_CHUNK)
+        r0, r1 = (0, R) if row_range is None else row_range
+        for t0 in range(r0, r1, _ROW_CHUNK):
+            t1 = min(r1, t0 + _ROW_CHUNK)
             t = np.arange(t0, t1)
             S = s * (Q[t0:t1, h, :] @ K.T)                           # [c, N]
             visible = np.arange(N)[None, :] <= (P + t)[:, None]

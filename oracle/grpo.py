@@ -59,19 +59,26 @@ def _ids(ids):
     return np.asarray(ids).astype(np.int64).reshape(-1)
 
 
+def _row_index(t, rows):
+    import torch
+    return torch.as_tensor(rows, dtype=torch.long, device=t.device)
+
+
 def _lse_rows(X):
     m = X.max(axis=1, keepdims=True)
     return (m + np.log(np.exp(X - m).sum(axis=1, keepdims=True)))[:, 0]
 
 
 def token_logp(logits, ids):
-    """log softmax(x)_y per row, float64.  logits [R, V], ids [R]."""
-    X = _f64(logits)
+    """log softmax(x)_y per row, float64.  logits [R, V], ids [R].  Rows are upcast to
+    float64 a chunk at a time, so a full response's logits need not fit in fp64 at once."""
     y = _ids(ids)
-    out = np.empty(X.shape[0])
-    for r0 in range(0, X.shape[0], _ROW_CHUNK):
-        r1 = min(X.shape[0], r0 + _ROW_CHUNK)
-        out[r0:r1] = X[np.arange(r0, r1), y[r0:r1]] - _lse_rows(X[r0:r1])
+    R = logits.shape[0]
+    out = np.empty(R)
+    for r0 in range(0, R, _ROW_CHUNK):
+        r1 = min(R, r0 + _ROW_CHUNK)
+        X = _f64(logits[r0:r1])
+        out[r0:r1] = X[np.arange(r1 - r0), y[r0:r1]] - _lse_rows(X)
     return out
 
 
@@ -93,19 +100,19 @@ def grpo_loss(logits, ids, logp_old, A, eps, G, rows=None):
     Returns dict(loss=scalar, logp [R], rho [R], clipped bool [R], dlogits [R, V] or the
     selected rows' [n, V] when `rows` is given).  The loss always covers every token.
     """
-    X = _f64(logits)
     y = _ids(ids)
     old = _f64(logp_old).reshape(-1)
-    R, V = X.shape
+    R, V = logits.shape
     A = float(A)
     coef = 1.0 / (G * R)
 
     logp = np.empty(R)
     lse = np.empty(R)
-    for r0 in range(0, R, _ROW_CHUNK):
+    for r0 in range(0, R, _ROW_CHUNK):       # rows upcast a chunk at a time
         r1 = min(R, r0 + _ROW_CHUNK)
-        lse[r0:r1] = _lse_rows(X[r0:r1])
-        logp[r0:r1] = X[np.arange(r0, r1), y[r0:r1]] - lse[r0:r1]
+        X = _f64(logits[r0:r1])
+        lse[r0:r1] = _lse_rows(X)
+        logp[r0:r1] = X[np.arange(r1 - r0), y[r0:r1]] - lse[r0:r1]
     rho = np.exp(logp - old)
     surr, clipped, dsurr = surrogate(rho, A, eps)
     loss = -coef * surr.sum()
@@ -116,7 +123,9 @@ def grpo_loss(logits, ids, logp_old, A, eps, G, rows=None):
     for k0 in range(0, len(sel), _ROW_CHUNK):
         k1 = min(len(sel), k0 + _ROW_CHUNK)
         rr = sel[k0:k1]
-        soft = np.exp(X[rr] - lse[rr, None])
+        Xr = _f64(logits[rr] if not hasattr(logits, "index_select") else
+                  logits.index_select(0, _row_index(logits, rr)))
+        soft = np.exp(Xr - lse[rr, None])
         onehot = np.zeros_like(soft)
         onehot[np.arange(len(rr)), y[rr]] = 1.0
         dlogits[k0:k1] = g[rr, None] * (onehot - soft)

@@ -183,3 +183,16 @@ def test_prompt_gradient_is_linear_in_the_group():
     b = att.replay_response(kp, vp, *resp[1])
     np.testing.assert_allclose(dk, a["dk_prefix"] + b["dk_prefix"], rtol=1e-14)
     np.testing.assert_allclose(dv, a["dv_prefix"] + b["dv_prefix"], rtol=1e-14)
+
+
+def test_row_range_gives_exact_tail_key_gradients():
+    """Suffix keys j >= t0 are seen only by rows t >= t0, so replaying just those rows
+    reproduces their key gradients (and those rows' outputs) exactly."""
+    c = _case(P=13, R=9, Hq=4, Hkv=2, D=5, seed=31)
+    full = att.replay_response(**c)
+    part = att.replay_response(**c, row_range=(6, 9))
+    np.testing.assert_allclose(part["o"][6:], full["o"][6:], rtol=1e-13)
+    np.testing.assert_allclose(part["dq"][6:], full["dq"][6:], rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(part["dk_suffix"][6:], full["dk_suffix"][6:], rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(part["dv_suffix"][6:], full["dv_suffix"][6:], rtol=1e-12, atol=1e-14)
+    assert np.all(part["o"][:6] == 0.0)
