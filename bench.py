@@ -34,6 +34,26 @@ def pairs(P, R):
     return R * P + R * (R + 1) // 2
 
 
+KERNELS_PER_BRACKET = {"zero": 2, "grpo_loss": 2, "finalize": 2}   # kernels one timed call launches
+
+
+def load_traffic(w, R_list):
+    """Per-launch DRAM traffic of the dK/dV kernel from the committed ncu capture, scaled by
+    work units (128-key tiles); None once the profiled kernel source has changed."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+            t = json.load(f)["bwd_dkdv"]
+        src = os.path.join(ROOT, t["kernel_source"])
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if sha != t["kernel_source_sha256_16"]:
+            return None
+        units = [w.Hkv * ((w.P + 127) // 128 + (R + 127) // 128) for R in R_list]
+        return t["dram_bytes_per_unit"] * sum(units) / len(units)
+    except Exception:
+        return None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -351,10 +371,11 @@ def run_ours(args, w):
                          "frac": ach / pk}
     dom = max(kernels, key=lambda k: kernels[k]["share"])
     d = kernels[dom]
+    traffic = load_traffic(w, grp.R) if dom == "bwd_dkdv" else None
     roofline = {"kernel": dom, "bound": d["bound"], "achieved": d["achieved"], "peak": d["peak"],
-                "unit": d["unit"], "frac": d["frac"], "traffic": None,
+                "unit": d["unit"], "frac": d["frac"], "traffic": traffic,
                 "peak_source": peak_src + (" sustained bf16" if d["bound"] == "tensor" else " HBM copy")}
-    launches = sum(v["launches"] for v in kernels.values())
+    launches = sum(v["launches"] * KERNELS_PER_BRACKET.get(k, 1) for k, v in kernels.items())
 
     # ---------------- end to end through the C ABI with host buffers
     e2e = None
