@@ -54,6 +54,26 @@ def load_traffic(w, R_list):
         return None
 
 
+def rank_max(x, dist=None, device="cpu"):
+    """Max of a per-rank scalar over all ranks (the job's time is its slowest rank's)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_sum(x, dist=None, device="cpu"):
+    """Sum of a per-rank scalar over all ranks (whole-job work)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t)
+    return float(t.item())
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -296,18 +316,10 @@ def run_ours(args, w):
             dist.barrier()
 
     def max_over_ranks(x):
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return rank_max(x, dist, dev)
 
     def sum_over_ranks(x):
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t)
-        return float(t.item())
+        return rank_sum(x, dist, dev)
 
     grp = Group(w, args.seed + rank, dev)
     losses = torch.zeros(args.warmup + 2 * args.steps + 2, dtype=torch.float64, device=dev)
