@@ -8,22 +8,27 @@
 //   dV = P^T dO,  dK = s dS^T Q,  dQ = s dS K.
 //
 // K3 attn_bwd_dkdv (key-tile outer): a work unit is one 128-key tile of one kv head, either
-//   a prompt tile or a suffix tile.  The unit sweeps every 64-row Q/dO sub-tile that sees
-//   its keys (qt64 = 64/g queries x g heads), computing S^T = K Q^T and dP^T = V dO^T into
-//   double-buffered TMEM, and accumulating dV += P^T dO and dK += dS^T Q in TMEM with P^T
-//   and dS^T written back to TMEM as bf16 (tcgen05.mma with A from TMEM).  The epilogue
-//   adds a prompt tile into the fp32 accumulators (read-modify-write by the one CTA that
-//   owns the tile: no atomics, stream-ordered across calls) or stores a suffix tile in bf16.
-// K4 attn_bwd_dq (query-tile outer): a work unit is one 128-row Q tile; it sweeps 64-key
+//   a prompt tile or a suffix tile.  It sweeps every 128-row Q/dO tile that sees its keys
+//   (qt = 128/g queries x the g heads of the kv head).  Per tile: S^T = K Q^T and
+//   dP^T = V dO^T into TMEM, the softmax turns them into bf16 P^T and dS^T, and
+//   dV += P^T dO, dK += dS^T Q accumulate in TMEM (tcgen05.mma with A from TMEM).  The
+//   epilogue adds a prompt tile into the fp32 accumulators (read-modify-write by the one CTA
+//   that owns the tile: no atomics, stream-ordered across calls) or stores a suffix tile.
+// K4 attn_bwd_dq (query-tile outer): a work unit is one 128-row Q tile; it sweeps 128-key
 //   steps over the prompt and the causal suffix, recomputing S and dP and accumulating
-//   dQ += dS K in TMEM.  Splitting dQ from dK/dV costs three extra MMAs per tile pair but
-//   removes every dQ atomic (the prompt dimension is ~170x the suffix at a 2M prompt).
+//   dQ += dS K in TMEM.  Splitting dQ from dK/dV costs recomputing S and dP but removes every
+//   dQ atomic (the prompt is ~170x the suffix at a 2M prompt).
 //
-// Both kernels: warp 0 = TMA producer, warp 1 = MMA issuer, warp 2 = TMEM owner,
-// warps 4-11 = two softmax warpgroups.  Both warpgroups work on every double-buffered TMEM
-// tile, each on half of its columns, which halves the softmax latency on the MMA's
-// critical path (S/dP of step j -> dS of step j -> the accumulate MMA of step j).
-// Every wait is bounded (status word + clean exit on timeout).
+// Every MMA is 128 x 128 (or 128 x D): narrower tcgen05 tiles run well below the tensor
+// rate.  TMEM holds one S and one dP tile; the overlap comes from where the softmax puts its
+// bf16 results: packed P/dS overwrite the fp32 dP columns the softmax has just read, so the
+// S columns are free as soon as S is in registers and the next tile's S = K Q^T (or Q K^T)
+// runs on the tensor pipe while the softmax works; the next dP is issued, in order, after
+// the MMAs that read P/dS.
+//
+// Warp roles (384 threads, one CTA per SM): warp 0 TMA producer, warp 1 one MMA-issuing
+// thread, warp 2 TMEM owner, warps 4-11 two softmax warpgroups; warpgroup w owns tile
+// columns [64 w, 64 w + 64).  Every wait is bounded (status word + clean exit on timeout).
 #include "ls_internal.h"
 #include "ptx.cuh"
 
@@ -33,44 +38,49 @@ namespace {
 constexpr int kThreads = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Column (within a 128-column TMEM region) of the packed bf16 A operand for k-step kk
+// (16 rows or keys): warpgroup kk / 4 wrote rows [64 w, 64 w + 64) as two 32-row chunks,
+// each chunk's 16 packed columns placed at the start of that chunk's own fp32 columns.
+__device__ __forceinline__ constexpr uint32_t packed_col(int kk) {
+  return 64u * (kk >> 2) + 32u * ((kk >> 1) & 1) + 8u * (kk & 1);
+}
+
 // =======================================================================================
 // K3: dK / dV
 // =======================================================================================
 template <int D>
 struct DkdvCfg {
   static constexpr int kBoxes = D / 64;
-  static constexpr int kKV = 128 * D * 2;         // K or V tile, 128 keys
-  static constexpr int kSub = 64 * D * 2;         // Q or dO sub-tile, 64 rows
-  static constexpr int kNS = 4;                   // sub-tile ring stages
-  static constexpr int kStage = 2 * kSub + 1024;  // Q, dO, row stats (512 B, padded)
-  static constexpr int kOffK = 0, kOffV = kKV, kOffStage = 2 * kKV;
+  static constexpr int kTile = 128 * D * 2;         // K, V, Q or dO tile (128 rows)
+  static constexpr int kNS = (D == 128) ? 2 : 4;    // Q/dO ring stages
+  static constexpr int kStage = 2 * kTile + 1024;   // Q, dO, row stats (LSE2[128], Delta[128])
+  static constexpr int kOffK = 0, kOffV = kTile, kOffStage = 2 * kTile;
   static constexpr int kOffBar = kOffStage + kNS * kStage;
   static constexpr int kBarKVFull = 0, kBarKVEmpty = 1, kBarQFull = 2;
   static constexpr int kBarQEmpty = kBarQFull + kNS;
   static constexpr int kBarSFull = kBarQEmpty + kNS;
-  static constexpr int kBarDSFull = kBarSFull + 2;
-  static constexpr int kBarAccDone = kBarDSFull + 2;
+  static constexpr int kBarSFree = kBarSFull + 1;
+  static constexpr int kBarDPFull = kBarSFree + 1;
+  static constexpr int kBarPDSFull = kBarDPFull + 1;
+  static constexpr int kBarAccDone = kBarPDSFull + 1;
   static constexpr int kBarAccFree = kBarAccDone + 1;
   static constexpr int kBarDrain = kBarAccFree + 1;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kSmem = kOffBar + kNumBars * 8 + 16 + 1024;
-  // TMEM: S^T_b at 64 b, dP^T_b at 128 + 64 b, dV at 256, dK at 256 + D.  Packed bf16
-  // P^T / dS^T of rows [32 w, 32 w + 32) alias columns [32 w, 32 w + 16) of S^T_b / dP^T_b.
-  __host__ __device__ static constexpr uint32_t col_s(int b) { return 64u * b; }
-  __host__ __device__ static constexpr uint32_t col_dp(int b) { return 128u + 64u * b; }
-  static constexpr uint32_t kColDV = 256u;
-  static constexpr uint32_t kColDK = 256u + D;
+  // TMEM: S^T at 0, dP^T at 128 (packed P^T at packed_col(kk), dS^T 16 columns further),
+  // dV at 256, dK at 256 + D.
+  static constexpr uint32_t kColS = 0u, kColDP = 128u, kColDV = 256u, kColDK = 256u + D;
 };
 
 struct KvUnit {
   int kv;
   bool prompt;
   int key0;   // first key of the tile (prompt or suffix index)
-  int i0;     // first 64-row sub-tile
-  int n;      // number of sub-tiles
+  int i0;     // first 128-row Q tile
+  int n;      // number of Q tiles
 };
 
-__device__ __forceinline__ KvUnit make_kv_unit(int u, const AttnShape& sh, int qt64, int n_q64) {
+__device__ __forceinline__ KvUnit make_kv_unit(int u, const AttnShape& sh, int n_qt) {
   const int n_pt = static_cast<int>((sh.P + 127) / 128);
   const int n_st = static_cast<int>((sh.R + 127) / 128);
   KvUnit w;
@@ -78,8 +88,8 @@ __device__ __forceinline__ KvUnit make_kv_unit(int u, const AttnShape& sh, int q
   const int j = u - w.kv * (n_pt + n_st);
   w.prompt = j < n_pt;
   w.key0 = w.prompt ? 128 * j : 128 * (j - n_pt);
-  w.i0 = w.prompt ? 0 : w.key0 / qt64;
-  w.n = n_q64 - w.i0;
+  w.i0 = w.prompt ? 0 : w.key0 / sh.qt;
+  w.n = n_qt - w.i0;
   return w;
 }
 
@@ -91,10 +101,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const __grid_constant__ CUtensorMap tm_vs,
                          const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_do, const AttnShape sh,
-                         const int qt64, const float2* __restrict__ rowstats,
-                         float* __restrict__ dk_acc, float* __restrict__ dv_acc,
-                         uint16_t* __restrict__ dk_suf, uint16_t* __restrict__ dv_suf,
-                         uint32_t* status) {
+                         const float* __restrict__ rowstats, float* __restrict__ dk_acc,
+                         float* __restrict__ dv_acc, uint16_t* __restrict__ dk_suf,
+                         uint16_t* __restrict__ dv_suf, uint32_t* status) {
   using C = DkdvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -104,25 +113,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_q64 = static_cast<int>((sh.R + qt64 - 1) / qt64);
-  const int n_units =
-      sh.Hkv * static_cast<int>((sh.P + 127) / 128 + (sh.R + 127) / 128);
-  const int rows_used = sh.g * qt64;   // rows of a 64-row sub-tile that TMA fills
+  const int n_qt = static_cast<int>((sh.R + sh.qt - 1) / sh.qt);
+  const int n_units = sh.Hkv * static_cast<int>((sh.P + 127) / 128 + (sh.R + 127) / 128);
+  const int rows_used = sh.g * sh.qt;   // rows of a 128-row tile that TMA fills
 
   // Padding rows of every Q/dO stage are never written by TMA: zero them once so that
   // they contribute exactly nothing to the sums over rows in dK and dV.
-  if (rows_used < 64) {
-    const int pad_rows = 64 - rows_used;
-    const int per_stage = 2 * C::kBoxes * pad_rows * 8;   // 16-byte chunks
-    for (int idx = threadIdx.x; idx < C::kNS * per_stage; idx += kThreads) {
-      const int st = idx / per_stage;
-      int rem = idx - st * per_stage;
-      const int buf = rem / (C::kBoxes * pad_rows * 8);   // 0 = Q, 1 = dO
-      rem -= buf * (C::kBoxes * pad_rows * 8);
+  if (rows_used < 128) {
+    const int pad_rows = 128 - rows_used;
+    const int per_buf = C::kBoxes * pad_rows * 8;   // 16-byte chunks per Q or dO buffer
+    for (int idx = threadIdx.x; idx < C::kNS * 2 * per_buf; idx += kThreads) {
+      const int st = idx / (2 * per_buf);
+      int rem = idx - st * 2 * per_buf;
+      const int buf = rem / per_buf;                 // 0 = Q, 1 = dO
+      rem -= buf * per_buf;
       const int box = rem / (pad_rows * 8);
       rem -= box * (pad_rows * 8);
       const int row = rows_used + rem / 8, chunk = rem & 7;
-      uint8_t* p = smem + C::kOffStage + st * C::kStage + buf * C::kSub + box * 8192 +
+      uint8_t* p = smem + C::kOffStage + st * C::kStage + buf * C::kTile + box * 16384 +
                    row * 128 + chunk * 16;
       *reinterpret_cast<uint4*>(p) = make_uint4(0u, 0u, 0u, 0u);
     }
@@ -136,10 +144,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars[C::kBarQFull + i], 1);
       mbar_init(&bars[C::kBarQEmpty + i], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars[C::kBarSFull + b], 1);
-      mbar_init(&bars[C::kBarDSFull + b], 256);
-    }
+    mbar_init(&bars[C::kBarSFull], 1);
+    mbar_init(&bars[C::kBarSFree], 256);
+    mbar_init(&bars[C::kBarDPFull], 1);
+    mbar_init(&bars[C::kBarPDSFull], 256);
     mbar_init(&bars[C::kBarAccDone], 1);
     mbar_init(&bars[C::kBarAccFree], 256);
     mbar_init(&bars[C::kBarDrain], 1);
@@ -155,9 +163,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   volatile int* vabort = &abort_flag;
-  const uint32_t q_tx = static_cast<uint32_t>(2 * C::kBoxes * 128 * rows_used + 512);
+  const uint32_t q_tx = static_cast<uint32_t>(2 * C::kBoxes * 128 * rows_used + 1024);
 
   if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_kp);
       tma_prefetch_desc(&tm_vp);
@@ -168,10 +177,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t qit = 0, uc = 0;
       bool ok = true, kv_pending = false;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
-        const KvUnit w = make_kv_unit(u, sh, qt64, n_q64);
+        const KvUnit w = make_kv_unit(u, sh, n_qt);
         if (uc > 0) ok = mbar_wait(&bars[C::kBarKVEmpty], (uc - 1) & 1u, status, vabort);
         if (!ok) break;
-        mbar_arrive_expect_tx(&bars[C::kBarKVFull], 2 * C::kKV);
+        mbar_arrive_expect_tx(&bars[C::kBarKVFull], 2 * C::kTile);
         for (int b = 0; b < C::kBoxes; ++b) {
           tma_load_3d(smem + C::kOffK + b * 16384, w.prompt ? &tm_kp : &tm_ks,
                       &bars[C::kBarKVFull], 64 * b, w.kv, w.key0);
@@ -188,13 +197,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* base = smem + C::kOffStage + st * C::kStage;
           mbar_arrive_expect_tx(&bars[C::kBarQFull + st], q_tx);
           for (int b = 0; b < C::kBoxes; ++b) {
-            tma_load_3d(base + b * 8192, &tm_q, &bars[C::kBarQFull + st], 64 * b, w.kv * sh.g,
-                        i * qt64);
-            tma_load_3d(base + C::kSub + b * 8192, &tm_do, &bars[C::kBarQFull + st], 64 * b,
-                        w.kv * sh.g, i * qt64);
+            tma_load_3d(base + b * 16384, &tm_q, &bars[C::kBarQFull + st], 64 * b, w.kv * sh.g,
+                        i * sh.qt);
+            tma_load_3d(base + C::kTile + b * 16384, &tm_do, &bars[C::kBarQFull + st], 64 * b,
+                        w.kv * sh.g, i * sh.qt);
           }
-          bulk_load(base + 2 * C::kSub, rowstats + (static_cast<int64_t>(w.kv) * n_q64 + i) * 64,
-                    512, &bars[C::kBarQFull + st]);
+          bulk_load(base + 2 * C::kTile, rowstats + (static_cast<int64_t>(w.kv) * n_qt + i) * 256,
+                    1024, &bars[C::kBarQFull + st]);
         }
       }
       if (!ok) {
@@ -206,77 +215,85 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_bf16(128, 64, false, false);
+      constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t kIdAcc = idesc_bf16(128, D, false, true);
-      const uint32_t sK = smem_u32(smem + C::kOffK), sV = smem_u32(smem + C::kOffV);
+      const uint64_t dK0 = smem_desc(smem_u32(smem + C::kOffK), 16, 1024);
+      const uint64_t dV0 = smem_desc(smem_u32(smem + C::kOffV), 16, 1024);
       const uint32_t sStage = smem_u32(smem + C::kOffStage);
-      uint32_t qit = 0, uc = 0, dsph = 0u;   // bit b: parity of the next wait on buffer b
+      const uint64_t dS0 = smem_desc(sStage, 16, 1024);      // K-major view of a stage
+      const uint64_t dM0 = smem_desc(sStage, 16384, 1024);   // MN-major view of a stage
+      uint32_t qit = 0, uc = 0, n_s = 0, n_pds = 0;
       bool ok = true;
-      const uint64_t dK0 = smem_desc(sK, 16, 1024), dV0 = smem_desc(sV, 16, 1024);
-      const uint64_t dS0 = smem_desc(sStage, 16, 1024);         // K-major view of a stage
-      const uint64_t dM0 = smem_desc(sStage, 8192, 1024);       // MN-major view of a stage
-      auto issue_s = [&](int b, uint32_t st) {
+      // S^T = K Q^T for the tile in stage st; waits until the softmax has taken the
+      // previous S out of TMEM
+      auto issue_s = [&](uint32_t st) -> bool {
+        if (n_s > 0 && !mbar_wait(&bars[C::kBarSFree], (n_s - 1) & 1u, status, vabort))
+          return false;
+        tc_fence_after();
         const uint64_t q = dS0 + static_cast<uint64_t>((st * C::kStage) >> 4);
-        const uint64_t o = q + static_cast<uint64_t>(C::kSub >> 4);
-        const uint32_t ds = tmem + C::col_s(b), dp = tmem + C::col_dp(b);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t oa = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-          const uint64_t ob = static_cast<uint64_t>(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4);
-          mma_bf16_ss(ds, dK0 + oa, q + ob, kIdS, kk > 0 ? 1u : 0u);
-          mma_bf16_ss(dp, dV0 + oa, o + ob, kIdS, kk > 0 ? 1u : 0u);
+          const uint64_t o = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+          mma_bf16_ss(tmem + C::kColS, dK0 + o, q + o, kIdS, kk > 0 ? 1u : 0u);
         }
+        mma_commit(&bars[C::kBarSFull]);
+        ++n_s;
+        return true;
       };
-      auto issue_acc = [&](int b, uint32_t st, bool acc) {
-        const uint64_t q = dM0 + static_cast<uint64_t>((st * C::kStage) >> 4);
-        const uint64_t o = q + static_cast<uint64_t>(C::kSub >> 4);
-        const uint32_t ps = tmem + C::col_s(b), pd = tmem + C::col_dp(b);
+      auto issue_dp = [&](uint32_t st) {
+        const uint64_t o_ = dS0 + static_cast<uint64_t>((st * C::kStage + C::kTile) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          // rows 16 kk .. 16 kk + 15: packed by warpgroup kk / 2 at column 32 (kk / 2)
-          const uint32_t ac = 32u * (kk >> 1) + 8u * (kk & 1);
-          const uint64_t ok_ = static_cast<uint64_t>((kk * 2048) >> 4);
-          mma_bf16_ts(tmem + C::kColDV, ps + ac, o + ok_, kIdAcc, (acc || kk > 0) ? 1u : 0u);
-          mma_bf16_ts(tmem + C::kColDK, pd + ac, q + ok_, kIdAcc, (acc || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t o = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+          mma_bf16_ss(tmem + C::kColDP, dV0 + o, o_ + o, kIdS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars[C::kBarDPFull]);
+      };
+      auto issue_acc = [&](uint32_t st, bool acc) {
+        const uint64_t q = dM0 + static_cast<uint64_t>((st * C::kStage) >> 4);
+        const uint64_t o = q + static_cast<uint64_t>(C::kTile >> 4);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ko = static_cast<uint64_t>((kk * 2048) >> 4);
+          const uint32_t pc = tmem + C::kColDP + packed_col(kk);
+          mma_bf16_ts(tmem + C::kColDV, pc, o + ko, kIdAcc, (acc || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + C::kColDK, pc + 16u, q + ko, kIdAcc, (acc || kk > 0) ? 1u : 0u);
         }
       };
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
-        const KvUnit w = make_kv_unit(u, sh, qt64, n_q64);
+        const KvUnit w = make_kv_unit(u, sh, n_qt);
         ok = mbar_wait(&bars[C::kBarKVFull], uc & 1u, status, vabort);
         if (!ok) break;
+        const uint32_t st0 = qit % C::kNS;
+        ok = mbar_wait(&bars[C::kBarQFull + st0], (qit / C::kNS) & 1u, status, vabort);
+        if (!ok) break;
         tc_fence_after();
-        const int npro = w.n < 2 ? w.n : 2;
-        for (int b = 0; b < npro && ok; ++b) {
-          const uint32_t st = (qit + b) % C::kNS;
-          ok = mbar_wait(&bars[C::kBarQFull + st], ((qit + b) / C::kNS) & 1u, status, vabort);
-          if (!ok) break;
-          tc_fence_after();
-          issue_s(b, st);
-          mma_commit(&bars[C::kBarSFull + b]);
-        }
+        ok = issue_s(st0);
+        if (!ok) break;
+        issue_dp(st0);
         for (int li = 0; li < w.n && ok; ++li) {
-          const int b = li & 1;
           const uint32_t st = (qit + li) % C::kNS;
-          ok = mbar_wait(&bars[C::kBarDSFull + b], (dsph >> b) & 1u, status, vabort);
+          const bool more = li + 1 < w.n;
+          const uint32_t st1 = (qit + li + 1) % C::kNS;
+          if (more) {
+            ok = mbar_wait(&bars[C::kBarQFull + st1], ((qit + li + 1) / C::kNS) & 1u, status,
+                           vabort);
+            if (ok) ok = issue_s(st1);
+            if (!ok) break;
+          }
+          ok = mbar_wait(&bars[C::kBarPDSFull], n_pds & 1u, status, vabort);
           if (!ok) break;
-          dsph ^= 1u << b;
+          ++n_pds;
           if (li == 0 && uc > 0) {
             ok = mbar_wait(&bars[C::kBarAccFree], (uc - 1) & 1u, status, vabort);
             if (!ok) break;
           }
           tc_fence_after();
-          issue_acc(b, st, li > 0);
+          issue_acc(st, li > 0);
           mma_commit(&bars[C::kBarQEmpty + st]);
-          if (li + 2 < w.n) {
-            const uint32_t st2 = (qit + li + 2) % C::kNS;
-            ok = mbar_wait(&bars[C::kBarQFull + st2], ((qit + li + 2) / C::kNS) & 1u, status,
-                           vabort);
-            if (!ok) break;
-            tc_fence_after();
-            issue_s(b, st2);
-            mma_commit(&bars[C::kBarSFull + b]);
-          }
+          if (more) issue_dp(st1);
         }
         if (!ok) break;
         qit += w.n;
@@ -288,69 +305,96 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_ns(&bars[C::kBarDrain], 0u, ok ? LS_WAIT_LIMIT_NS : 200000000ull);
     }
   } else if (warp >= 4) {
+    // ------------------------------------------------------------------ softmax warpgroups
     const int wg = (warp - 4) >> 2;
     const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;   // key within the tile
+    const int row = quarter * 32 + lane;   // key within the tile (TMEM lane)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float c2 = sh.scale * kLog2e;
-    uint32_t sph = 0u, qit = 0u, uc = 0u;   // bit b: parity of the next wait on buffer b
+    uint32_t qit = 0u, uc = 0u, n_tiles = 0u;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
-      const KvUnit w = make_kv_unit(u, sh, qt64, n_q64);
+      const KvUnit w = make_kv_unit(u, sh, n_qt);
       const int key = w.key0 + row;
-      // both warpgroups work on every sub-tile: warpgroup wg owns its rows [32 wg, 32 wg + 32)
-      for (int li = 0; li < w.n; ++li) {
-        const int b = li & 1;
+      for (int li = 0; li < w.n; ++li, ++n_tiles) {
         const uint32_t st = (qit + li) % C::kNS;
-        ok = mbar_wait(&bars[C::kBarSFull + b], (sph >> b) & 1u, status, vabort);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        sph ^= 1u << b;
-        // acquire the row stats copied into this stage (long complete: the MMA waited on it)
-        ok = mbar_wait(&bars[C::kBarQFull + st], ((qit + li) / C::kNS) & 1u, status, vabort);
+        ok = mbar_wait(&bars[C::kBarSFull], n_tiles & 1u, status, vabort);
+        if (ok)   // acquire this stage's row stats (long complete: the MMA waited on it)
+          ok = mbar_wait(&bars[C::kBarQFull + st], ((qit + li) / C::kNS) & 1u, status, vabort);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        const float4* rs4 = reinterpret_cast<const float4*>(smem + C::kOffStage + st * C::kStage +
-                                                            2 * C::kSub);
-        // causal suffix: rows r < lo see only suffix keys < this key
-        int lo = 0;
+        const float* rs = reinterpret_cast<const float*>(smem + C::kOffStage + st * C::kStage +
+                                                         2 * C::kTile);
+        const float4* lse4 = reinterpret_cast<const float4*>(rs) + wg * 16;   // rows 64 wg ..
+        const float4* dlt4 = reinterpret_cast<const float4*>(rs + 128) + wg * 16;
+        // ---- P^T from S^T (this warpgroup's 64 rows); S leaves TMEM first
+        float p[64];
+        {
+          uint32_t sa[32], sb[32];
+          tmem_ld32(lane_base + C::kColS + wg * 64, sa);
+          tmem_ld32(lane_base + C::kColS + wg * 64 + 32, sb);
+          tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(&bars[C::kBarSFree]);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 l4 = lse4[i];
+            p[4 * i + 0] = ex2_approx(fmaf(__uint_as_float(sa[4 * i + 0]), c2, -l4.x));
+            p[4 * i + 1] = ex2_approx(fmaf(__uint_as_float(sa[4 * i + 1]), c2, -l4.y));
+            p[4 * i + 2] = ex2_approx(fmaf(__uint_as_float(sa[4 * i + 2]), c2, -l4.z));
+            p[4 * i + 3] = ex2_approx(fmaf(__uint_as_float(sa[4 * i + 3]), c2, -l4.w));
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 l4 = lse4[8 + i];
+            p[32 + 4 * i + 0] = ex2_approx(fmaf(__uint_as_float(sb[4 * i + 0]), c2, -l4.x));
+            p[32 + 4 * i + 1] = ex2_approx(fmaf(__uint_as_float(sb[4 * i + 1]), c2, -l4.y));
+            p[32 + 4 * i + 2] = ex2_approx(fmaf(__uint_as_float(sb[4 * i + 2]), c2, -l4.z));
+            p[32 + 4 * i + 3] = ex2_approx(fmaf(__uint_as_float(sb[4 * i + 3]), c2, -l4.w));
+          }
+        }
+        // causal suffix: rows r < lo of the tile see only suffix keys < this key
         if (!w.prompt) {
-          const int v = sh.g * (key - (w.i0 + li) * qt64);
-          lo = v < 0 ? 0 : (v > 64 ? 64 : v);
-        }
-        uint32_t sv[32], dv[32];
-        tmem_ld32(lane_base + C::col_s(b) + wg * 32, sv);
-        tmem_ld32(lane_base + C::col_dp(b) + wg * 32, dv);
-        tmem_ld_wait();
-        float p[32];
+          const int v = sh.g * (key - (w.i0 + li) * sh.qt);
+          const int lo = v < 0 ? 0 : (v > 128 ? 128 : v);
+          if (lo > wg * 64) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float4 st4 = rs4[wg * 16 + i];   // (LSE2, Delta) of rows c and c + 1
-          p[2 * i] = ex2_approx(fmaf(__uint_as_float(sv[2 * i]), c2, -st4.x));
-          p[2 * i + 1] = ex2_approx(fmaf(__uint_as_float(sv[2 * i + 1]), c2, -st4.z));
-          dv[2 * i] = __float_as_uint(__uint_as_float(dv[2 * i]) - st4.y);
-          dv[2 * i + 1] = __float_as_uint(__uint_as_float(dv[2 * i + 1]) - st4.w);
+            for (int i = 0; i < 64; ++i)
+              if (wg * 64 + i < lo) p[i] = 0.0f;
+          }
         }
-        if (lo > wg * 32) {
+        // ---- dS^T from dP^T; packed P^T / dS^T replace the fp32 dP^T chunk just read
+        ok = mbar_wait(&bars[C::kBarDPFull], (n_tiles & 1u), status, vabort);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (wg * 32 + i < lo) p[i] = 0.0f;
-        }
-        uint32_t pw[16], dw[16];
+        for (int ch = 0; ch < 2; ++ch) {
+          uint32_t dv[32];
+          const uint32_t col = C::kColDP + wg * 64 + ch * 32;
+          tmem_ld32(lane_base + col, dv);
+          tmem_ld_wait();
+          uint32_t pw[16], dw[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          pw[i] = pack_bf16x2(p[2 * i], p[2 * i + 1]);
-          dw[i] = pack_bf16x2(p[2 * i] * __uint_as_float(dv[2 * i]),
-                              p[2 * i + 1] * __uint_as_float(dv[2 * i + 1]));
+          for (int i = 0; i < 8; ++i) {
+            const float4 d4 = dlt4[ch * 8 + i];
+            const int c = ch * 32 + 4 * i;
+            const float s0 = p[c + 0] * (__uint_as_float(dv[4 * i + 0]) - d4.x);
+            const float s1 = p[c + 1] * (__uint_as_float(dv[4 * i + 1]) - d4.y);
+            const float s2 = p[c + 2] * (__uint_as_float(dv[4 * i + 2]) - d4.z);
+            const float s3 = p[c + 3] * (__uint_as_float(dv[4 * i + 3]) - d4.w);
+            pw[2 * i] = pack_bf16x2(p[c + 0], p[c + 1]);
+            pw[2 * i + 1] = pack_bf16x2(p[c + 2], p[c + 3]);
+            dw[2 * i] = pack_bf16x2(s0, s1);
+            dw[2 * i + 1] = pack_bf16x2(s2, s3);
+          }
+          tmem_st16(lane_base + col, pw);
+          tmem_st16(lane_base + col + 16, dw);
         }
-        // packed P^T / dS^T go to the first 16 of this warpgroup's own 32 columns, so no
-        // write can land on fp32 columns the other warpgroup has yet to read
-        tmem_st16(lane_base + C::col_s(b) + wg * 32, pw);
-        tmem_st16(lane_base + C::col_dp(b) + wg * 32, dw);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bars[C::kBarDSFull + b]);
+        mbar_arrive(&bars[C::kBarPDSFull]);
       }
       if (!ok) break;
       qit += w.n;
@@ -414,48 +458,45 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 struct DqCfg {
   static constexpr int kBoxes = D / 64;
-  static constexpr int kQ = 128 * D * 2;           // Q or dO tile, 128 rows
-  static constexpr int kKV = 64 * D * 2;           // K or V step tile, 64 keys
-  static constexpr int kNS = (D == 128) ? 4 : 8;   // K/V ring stages
-  static constexpr int kStage = 2 * kKV;
-  static constexpr int kOffQ = 0, kOffDO = kQ, kOffStage = 2 * kQ;
+  static constexpr int kTile = 128 * D * 2;         // Q, dO, K or V tile (128 rows)
+  static constexpr int kNS = (D == 128) ? 2 : 4;    // K/V ring stages
+  static constexpr int kStage = 2 * kTile;
+  static constexpr int kOffQ = 0, kOffDO = kTile, kOffStage = 2 * kTile;
   static constexpr int kOffBar = kOffStage + kNS * kStage;
   static constexpr int kBarQFull = 0, kBarQEmpty = 1, kBarQTmem = 2, kBarKVFull = 3;
   static constexpr int kBarKVEmpty = kBarKVFull + kNS;
   static constexpr int kBarSFull = kBarKVEmpty + kNS;
-  static constexpr int kBarDSFull = kBarSFull + 2;
-  static constexpr int kBarDQDone = kBarDSFull + 2;
+  static constexpr int kBarSFree = kBarSFull + 1;
+  static constexpr int kBarDPFull = kBarSFree + 1;
+  static constexpr int kBarDSFull = kBarDPFull + 1;
+  static constexpr int kBarDQDone = kBarDSFull + 1;
   static constexpr int kBarDQFree = kBarDQDone + 1;
   static constexpr int kBarDrain = kBarDQFree + 1;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kSmem = kOffBar + kNumBars * 8 + 16 + 1024;
-  // TMEM: S_b at 64 b (packed dS of keys [32 w, 32 w + 32) aliases its columns
-  // [32 w, 32 w + 16)), dP_b at 128 + 64 b, dQ at 256,
-  // and the unit's Q and dO rows (bf16, the A operand of S = Q K^T and dP = dO V^T) at
-  // 384 and 384 + D/2, so those MMAs read only the 64-key K/V tile from shared memory.
-  __host__ __device__ static constexpr uint32_t col_s(int b) { return 64u * b; }
-  __host__ __device__ static constexpr uint32_t col_dp(int b) { return 128u + 64u * b; }
-  static constexpr uint32_t kColDQ = 256u;
-  static constexpr uint32_t kColQ = 384u;
-  static constexpr uint32_t kColDO = 384u + D / 2;
+  // TMEM: S at 0, dP at 128 (packed dS at packed_col(kk)), dQ at 256, and the unit's Q and
+  // dO rows (bf16, the A operand of S = Q K^T and dP = dO V^T) at 384 and 384 + D/2.
+  static constexpr uint32_t kColS = 0u, kColDP = 128u, kColDQ = 256u;
+  static constexpr uint32_t kColQ = 384u, kColDO = 384u + D / 2;
 };
 
 struct QUnit {
   int kv;
   int t0;      // first query of the tile
-  int n_pt;    // prompt 64-key steps
+  int i;       // tile index
+  int n_pt;    // prompt 128-key steps
   int n;       // total steps
 };
 
 __device__ __forceinline__ QUnit make_q_unit(int u, const AttnShape& sh, int n_qt) {
   QUnit w;
   w.kv = u / n_qt;
-  const int i = u - w.kv * n_qt;
-  w.t0 = i * sh.qt;
+  w.i = u - w.kv * n_qt;
+  w.t0 = w.i * sh.qt;
   int t_end = w.t0 + sh.qt;
   if (t_end > sh.R) t_end = static_cast<int>(sh.R);
-  w.n_pt = static_cast<int>((sh.P + 63) / 64);
-  w.n = w.n_pt + (t_end + 63) / 64;
+  w.n_pt = static_cast<int>((sh.P + 127) / 128);
+  w.n = w.n_pt + (t_end + 127) / 128;
   return w;
 }
 
@@ -467,8 +508,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tm_vs,
                        const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_do, const AttnShape sh,
-                       const int qt64, const float2* __restrict__ rowstats,
-                       uint16_t* __restrict__ dq, uint32_t* status) {
+                       const float* __restrict__ rowstats, uint16_t* __restrict__ dq,
+                       uint32_t* status) {
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -479,7 +520,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_qt = static_cast<int>((sh.R + sh.qt - 1) / sh.qt);
-  const int n_q64 = static_cast<int>((sh.R + qt64 - 1) / qt64);
   const int n_units = sh.Hkv * n_qt;
 
   if (threadIdx.x == 0) {
@@ -491,10 +531,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars[C::kBarKVFull + i], 1);
       mbar_init(&bars[C::kBarKVEmpty + i], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars[C::kBarSFull + b], 1);
-      mbar_init(&bars[C::kBarDSFull + b], 256);
-    }
+    mbar_init(&bars[C::kBarSFull], 1);
+    mbar_init(&bars[C::kBarSFree], 256);
+    mbar_init(&bars[C::kBarDPFull], 1);
+    mbar_init(&bars[C::kBarDSFull], 256);
     mbar_init(&bars[C::kBarDQDone], 1);
     mbar_init(&bars[C::kBarDQFree], 256);
     mbar_init(&bars[C::kBarDrain], 1);
@@ -512,6 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* vabort = &abort_flag;
 
   if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_kp);
       tma_prefetch_desc(&tm_vp);
@@ -539,13 +580,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = mbar_wait(&bars[C::kBarKVEmpty + st], ((kit / C::kNS) - 1) & 1u, status, vabort);
           if (!ok) break;
           const bool pre = j < w.n_pt;
-          const int key0 = pre ? 64 * j : 64 * (j - w.n_pt);
+          const int key0 = pre ? 128 * j : 128 * (j - w.n_pt);
           uint8_t* base = smem + C::kOffStage + st * C::kStage;
-          mbar_arrive_expect_tx(&bars[C::kBarKVFull + st], 2 * C::kKV);
+          mbar_arrive_expect_tx(&bars[C::kBarKVFull + st], 2 * C::kTile);
           for (int b = 0; b < C::kBoxes; ++b) {
-            tma_load_3d(base + b * 8192, pre ? &tm_kp : &tm_ks, &bars[C::kBarKVFull + st], 64 * b,
-                        w.kv, key0);
-            tma_load_3d(base + C::kKV + b * 8192, pre ? &tm_vp : &tm_vs,
+            tma_load_3d(base + b * 16384, pre ? &tm_kp : &tm_ks, &bars[C::kBarKVFull + st],
+                        64 * b, w.kv, key0);
+            tma_load_3d(base + C::kTile + b * 16384, pre ? &tm_vp : &tm_vs,
                         &bars[C::kBarKVFull + st], 64 * b, w.kv, key0);
           }
         }
@@ -558,69 +599,79 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_bf16(128, 64, false, false);
+      constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t kIdQ = idesc_bf16(128, D, false, true);
       const uint32_t sStage = smem_u32(smem + C::kOffStage);
-      const uint64_t dK0 = smem_desc(sStage, 16, 1024);     // K-major view of a stage
-      const uint64_t dM0 = smem_desc(sStage, 8192, 1024);   // MN-major view of a stage
-      uint32_t kit = 0, uc = 0, dsph = 0u;   // bit b: parity of the next wait on buffer b
+      const uint64_t dK0 = smem_desc(sStage, 16, 1024);      // K-major view of a stage
+      const uint64_t dM0 = smem_desc(sStage, 16384, 1024);   // MN-major view of a stage
+      uint32_t kit = 0, uc = 0, n_s = 0, n_ds = 0;
       bool ok = true;
-      auto issue_s = [&](int b, uint32_t st) {
+      auto issue_s = [&](uint32_t st) -> bool {
+        if (n_s > 0 && !mbar_wait(&bars[C::kBarSFree], (n_s - 1) & 1u, status, vabort))
+          return false;
+        tc_fence_after();
         const uint64_t k = dK0 + static_cast<uint64_t>((st * C::kStage) >> 4);
-        const uint64_t v = k + static_cast<uint64_t>(C::kKV >> 4);
-        const uint32_t ds = tmem + C::col_s(b), dp = tmem + C::col_dp(b);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t ob = static_cast<uint64_t>(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4);
-          mma_bf16_ts(ds, tmem + C::kColQ + kk * 8, k + ob, kIdS, kk > 0 ? 1u : 0u);
-          mma_bf16_ts(dp, tmem + C::kColDO + kk * 8, v + ob, kIdS, kk > 0 ? 1u : 0u);
+          const uint64_t o = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+          mma_bf16_ts(tmem + C::kColS, tmem + C::kColQ + kk * 8, k + o, kIdS, kk > 0 ? 1u : 0u);
         }
+        mma_commit(&bars[C::kBarSFull]);
+        ++n_s;
+        return true;
       };
-      auto issue_dq = [&](int b, uint32_t st, bool acc) {
-        const uint64_t k = dM0 + static_cast<uint64_t>((st * C::kStage) >> 4);
-        const uint32_t a = tmem + C::col_s(b);
+      auto issue_dp = [&](uint32_t st) {
+        const uint64_t v = dK0 + static_cast<uint64_t>((st * C::kStage + C::kTile) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)   // keys 16 kk ..: packed by warpgroup kk / 2 at column 32 (kk / 2)
-          mma_bf16_ts(tmem + C::kColDQ, a + 32u * (kk >> 1) + 8u * (kk & 1),
-                      k + static_cast<uint64_t>((kk * 2048) >> 4), kIdQ, (acc || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t o = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+          mma_bf16_ts(tmem + C::kColDP, tmem + C::kColDO + kk * 8, v + o, kIdS,
+                      kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars[C::kBarDPFull]);
+      };
+      auto issue_dq = [&](uint32_t st, bool acc) {
+        const uint64_t k = dM0 + static_cast<uint64_t>((st * C::kStage) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16_ts(tmem + C::kColDQ, tmem + C::kColDP + packed_col(kk),
+                      k + static_cast<uint64_t>((kk * 2048) >> 4), kIdQ,
+                      (acc || kk > 0) ? 1u : 0u);
       };
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
         const QUnit w = make_q_unit(u, sh, n_qt);
         ok = mbar_wait(&bars[C::kBarQTmem], uc & 1u, status, vabort);
         if (!ok) break;
+        const uint32_t st0 = kit % C::kNS;
+        ok = mbar_wait(&bars[C::kBarKVFull + st0], (kit / C::kNS) & 1u, status, vabort);
+        if (!ok) break;
         tc_fence_after();
-        const int npro = w.n < 2 ? w.n : 2;
-        for (int b = 0; b < npro && ok; ++b) {
-          const uint32_t st = (kit + b) % C::kNS;
-          ok = mbar_wait(&bars[C::kBarKVFull + st], ((kit + b) / C::kNS) & 1u, status, vabort);
-          if (!ok) break;
-          tc_fence_after();
-          issue_s(b, st);
-          mma_commit(&bars[C::kBarSFull + b]);
-        }
+        ok = issue_s(st0);
+        if (!ok) break;
+        issue_dp(st0);
         for (int j = 0; j < w.n && ok; ++j) {
-          const int b = j & 1;
           const uint32_t st = (kit + j) % C::kNS;
-          ok = mbar_wait(&bars[C::kBarDSFull + b], (dsph >> b) & 1u, status, vabort);
+          const bool more = j + 1 < w.n;
+          const uint32_t st1 = (kit + j + 1) % C::kNS;
+          if (more) {
+            ok = mbar_wait(&bars[C::kBarKVFull + st1], ((kit + j + 1) / C::kNS) & 1u, status,
+                           vabort);
+            if (ok) ok = issue_s(st1);
+            if (!ok) break;
+          }
+          ok = mbar_wait(&bars[C::kBarDSFull], n_ds & 1u, status, vabort);
           if (!ok) break;
-          dsph ^= 1u << b;
+          ++n_ds;
           if (j == 0 && uc > 0) {
             ok = mbar_wait(&bars[C::kBarDQFree], (uc - 1) & 1u, status, vabort);
             if (!ok) break;
           }
           tc_fence_after();
-          issue_dq(b, st, j > 0);
+          issue_dq(st, j > 0);
           mma_commit(&bars[C::kBarKVEmpty + st]);
-          if (j + 2 < w.n) {
-            const uint32_t st2 = (kit + j + 2) % C::kNS;
-            ok = mbar_wait(&bars[C::kBarKVFull + st2], ((kit + j + 2) / C::kNS) & 1u, status,
-                           vabort);
-            if (!ok) break;
-            tc_fence_after();
-            issue_s(b, st2);
-            mma_commit(&bars[C::kBarSFull + b]);
-          }
+          if (more) issue_dp(st1);
         }
         if (!ok) break;
         kit += w.n;
@@ -631,23 +682,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_ns(&bars[C::kBarDrain], 0u, ok ? LS_WAIT_LIMIT_NS : 200000000ull);
     }
   } else if (warp >= 4) {
+    // ------------------------------------------------------------------ softmax warpgroups
     const int wg = (warp - 4) >> 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float c2 = sh.scale * kLog2e;
-    uint32_t sph = 0u, uc = 0u;   // bit b: parity of the next wait on buffer b
+    uint32_t uc = 0u, n_steps = 0u;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
       const QUnit w = make_q_unit(u, sh, n_qt);
       const int t = w.t0 + row / sh.g;
       const int hg = row % sh.g;
       const bool valid = (row < sh.g * sh.qt) && (t < sh.R);
-      float2 st2 = make_float2(INFINITY, 0.0f);
+      float lse2 = INFINITY, dlt = 0.0f;
       if (valid) {
-        const int i64 = t / qt64;
-        const int r64 = (t - i64 * qt64) * sh.g + hg;
-        st2 = rowstats[(static_cast<int64_t>(w.kv) * n_q64 + i64) * 64 + r64];
+        const float* rs = rowstats + (static_cast<int64_t>(w.kv) * n_qt + w.i) * 256;
+        lse2 = rs[row];
+        dlt = rs[128 + row];
       }
       // stage this unit's Q (warpgroup 0) or dO (warpgroup 1) row into TMEM; the previous
       // unit's MMAs have all completed (its dQ-done barrier was waited on)
@@ -675,46 +727,61 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&bars[C::kBarQTmem]);
         mbar_arrive(&bars[C::kBarQEmpty]);
       }
-      // both warpgroups work on every step: warpgroup wg owns key columns [32 wg, 32 wg + 32)
-      for (int j = 0; j < w.n; ++j) {
-        const int b = j & 1;
-        ok = mbar_wait(&bars[C::kBarSFull + b], (sph >> b) & 1u, status, vabort);
+      for (int j = 0; j < w.n; ++j, ++n_steps) {
+        ok = mbar_wait(&bars[C::kBarSFull], n_steps & 1u, status, vabort);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        sph ^= 1u << b;
         tc_fence_after();
-        int lim = 64;
+        // valid key columns of this row in this step
+        int lim = 128;
         if (j < w.n_pt) {
-          const int64_t rem = sh.P - 64ll * j;
-          if (rem < 64) lim = static_cast<int>(rem);
+          const int64_t rem = sh.P - 128ll * j;
+          if (rem < 128) lim = static_cast<int>(rem);
         } else {
-          const int v = t - 64 * (j - w.n_pt) + 1;
-          lim = v < 0 ? 0 : (v > 64 ? 64 : v);
+          const int v = t - 128 * (j - w.n_pt) + 1;
+          lim = v < 0 ? 0 : (v > 128 ? 128 : v);
         }
-        uint32_t sv[32], dv[32];
-        tmem_ld32(lane_base + C::col_s(b) + wg * 32, sv);
-        tmem_ld32(lane_base + C::col_dp(b) + wg * 32, dv);
-        tmem_ld_wait();
-        float p[32];
+        // ---- P from S (this warpgroup's 64 keys); S leaves TMEM first
+        float p[64];
+        {
+          uint32_t sa[32], sb[32];
+          tmem_ld32(lane_base + C::kColS + wg * 64, sa);
+          tmem_ld32(lane_base + C::kColS + wg * 64 + 32, sb);
+          tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(&bars[C::kBarSFree]);
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          p[i] = ex2_approx(fmaf(__uint_as_float(sv[i]), c2, -st2.x));
-        if (lim < wg * 32 + 32) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (wg * 32 + i >= lim) p[i] = 0.0f;
+          for (int i = 0; i < 32; ++i) {
+            p[i] = ex2_approx(fmaf(__uint_as_float(sa[i]), c2, -lse2));
+            p[32 + i] = ex2_approx(fmaf(__uint_as_float(sb[i]), c2, -lse2));
+          }
         }
-        uint32_t dw[16];
+        if (lim < wg * 64 + 64) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          dw[i] = pack_bf16x2(p[2 * i] * (__uint_as_float(dv[2 * i]) - st2.y),
-                              p[2 * i + 1] * (__uint_as_float(dv[2 * i + 1]) - st2.y));
-        // packed dS goes to the first 16 of this warpgroup's own 32 columns (no write lands
-        // on fp32 columns the other warpgroup has yet to read)
-        tmem_st16(lane_base + C::col_s(b) + wg * 32, dw);
+          for (int i = 0; i < 64; ++i)
+            if (wg * 64 + i >= lim) p[i] = 0.0f;
+        }
+        // ---- dS from dP; packed dS replaces the fp32 dP chunk just read
+        ok = mbar_wait(&bars[C::kBarDPFull], n_steps & 1u, status, vabort);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+          uint32_t dv[32];
+          const uint32_t col = C::kColDP + wg * 64 + ch * 32;
+          tmem_ld32(lane_base + col, dv);
+          tmem_ld_wait();
+          uint32_t dw[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            dw[i] = pack_bf16x2(p[ch * 32 + 2 * i] * (__uint_as_float(dv[2 * i]) - dlt),
+                                p[ch * 32 + 2 * i + 1] * (__uint_as_float(dv[2 * i + 1]) - dlt));
+          tmem_st16(lane_base + col, dw);
+        }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bars[C::kBarDSFull + b]);
+        mbar_arrive(&bars[C::kBarDSFull]);
       }
       if (!ok) break;
       // epilogue: dQ * s -> bf16; warpgroup 0 stores columns [0, D/2), warpgroup 1 the rest
@@ -767,12 +834,13 @@ cudaError_t launch_dkdv_d(const BwdArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int64_t n_units = static_cast<int64_t>(a.sh.Hkv) * ((a.sh.P + 127) / 128 + (a.sh.R + 127) / 128);
+  const int64_t n_units =
+      static_cast<int64_t>(a.sh.Hkv) * ((a.sh.P + 127) / 128 + (a.sh.R + 127) / 128);
   int grid = num_sms();
   if (n_units < grid) grid = static_cast<int>(n_units);
   attn_bwd_dkdv_kernel<D><<<grid, kThreads, C::kSmem, s>>>(
-      *a.tm_kp128, *a.tm_vp128, a.tm_ks128, a.tm_vs128, a.tm_q64, a.tm_do64, a.sh, a.qt64,
-      a.rowstats, a.dk_acc, a.dv_acc, a.dk_suf, a.dv_suf, a.status);
+      *a.tm_kp, *a.tm_vp, a.tm_ks, a.tm_vs, a.tm_q, a.tm_do, a.sh, a.rowstats, a.dk_acc,
+      a.dv_acc, a.dk_suf, a.dv_suf, a.status);
   return cudaGetLastError();
 }
 
@@ -789,9 +857,9 @@ cudaError_t launch_dq_d(const BwdArgs& a, cudaStream_t s) {
   const int64_t n_units = static_cast<int64_t>(a.sh.Hkv) * ((a.sh.R + a.sh.qt - 1) / a.sh.qt);
   int grid = num_sms();
   if (n_units < grid) grid = static_cast<int>(n_units);
-  attn_bwd_dq_kernel<D><<<grid, kThreads, C::kSmem, s>>>(*a.tm_kp64, *a.tm_vp64, a.tm_ks64,
-                                                        a.tm_vs64, a.tm_q128, a.tm_do128, a.sh,
-                                                        a.qt64, a.rowstats, a.dq, a.status);
+  attn_bwd_dq_kernel<D><<<grid, kThreads, C::kSmem, s>>>(*a.tm_kp, *a.tm_vp, a.tm_ks, a.tm_vs,
+                                                        a.tm_q, a.tm_do, a.sh, a.rowstats, a.dq,
+                                                        a.status);
   return cudaGetLastError();
 }
 

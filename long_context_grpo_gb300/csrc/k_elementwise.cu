@@ -3,7 +3,7 @@
 //   K7 finalize        out = scale * acc (bf16 or fp32), optionally zeroing acc: the group's
 //                      one finalization (LongStraw review, section 2-1 step 5)
 //   K2 bwd_prep        Delta[t,h] = sum_d dO[t,h,d] O[t,h,d], the row term of the softmax
-//                      backward dS = P * (dP - Delta), packed with LSE by 64-row sub-tile
+//                      backward dS = P * (dP - Delta), packed with LSE by 128-row Q tile
 // All use 128-bit accesses on a grid sized to the SM count.
 #include "ls_internal.h"
 
@@ -54,25 +54,26 @@ __global__ void __launch_bounds__(kThreads) scale_kernel(float4* acc, size_t n4,
   }
 }
 
-// One warp per 64-row sub-tile slot (kv, i, r): row r of sub-tile i packs query
-// t = i * qt64 + r / g and head h = kv * g + r % g.  Valid rows get
-// (LSE * log2 e, Delta = sum_d dO * O); padding rows and rows past R get (+inf, 0).
+// One warp per 128-row Q tile slot (kv, i, r): row r of tile i packs query
+// t = i * qt + r / g and head h = kv * g + r % g.  Valid rows get LSE log2 e and
+// Delta = sum_d dO O; padding rows and rows past R get (+inf, 0).  Layout per tile: the
+// 128 LSE values, then the 128 Delta values.
 __global__ void __launch_bounds__(kThreads) bwd_prep_kernel(const uint4* o, const uint4* d_out,
-                                                           const float* lse, float2* rowstats,
-                                                           AttnShape sh, int qt64, int64_t n_q64) {
+                                                           const float* lse, float* rowstats,
+                                                           AttnShape sh, int64_t n_qt) {
   const int lane = threadIdx.x & 31;
   const int64_t warps_total = static_cast<int64_t>(gridDim.x) * (kThreads / 32);
   const int per_row = sh.D / 8;   // 8 or 16 lanes, 8 bf16 each
-  const int64_t slots = static_cast<int64_t>(sh.Hkv) * n_q64 * 64;
+  const int64_t slots = static_cast<int64_t>(sh.Hkv) * n_qt * 128;
   for (int64_t sidx = blockIdx.x * static_cast<int64_t>(kThreads / 32) + (threadIdx.x >> 5);
        sidx < slots; sidx += warps_total) {
-    const int64_t kv = sidx / (n_q64 * 64);
-    const int64_t rem = sidx - kv * n_q64 * 64;
-    const int64_t i = rem >> 6;
-    const int r = static_cast<int>(rem & 63);
-    const int64_t t = i * qt64 + r / sh.g;
+    const int64_t tile = sidx >> 7;                // kv * n_qt + i
+    const int r = static_cast<int>(sidx & 127);
+    const int64_t kv = tile / n_qt;
+    const int64_t i = tile - kv * n_qt;
+    const int64_t t = i * sh.qt + r / sh.g;
     const int64_t h = kv * sh.g + r % sh.g;
-    const bool valid = (r < sh.g * qt64) && (t < sh.R);
+    const bool valid = (r < sh.g * sh.qt) && (t < sh.R);
     float acc = 0.f;
     if (valid && lane < per_row) {
       const int64_t row = t * sh.Hq + h;
@@ -89,15 +90,9 @@ __global__ void __launch_bounds__(kThreads) bwd_prep_kernel(const uint4* o, cons
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (lane == 0) {
-      float2 v;
-      if (valid) {
-        v.x = lse[t * sh.Hq + h] * 1.4426950408889634f;
-        v.y = acc;
-      } else {
-        v.x = INFINITY;
-        v.y = 0.f;
-      }
-      rowstats[sidx] = v;
+      float* dst = rowstats + tile * 256;
+      dst[r] = valid ? lse[t * sh.Hq + h] * 1.4426950408889634f : INFINITY;
+      dst[128 + r] = valid ? acc : 0.f;
     }
   }
 }
@@ -139,12 +134,12 @@ cudaError_t launch_scale_inplace(float* acc, size_t n, float scale, cudaStream_t
 }
 
 cudaError_t launch_bwd_prep(const uint16_t* o, const uint16_t* d_out, const float* lse,
-                            float2* rowstats, const AttnShape& sh, int qt64, cudaStream_t s) {
-  const int64_t n_q64 = (sh.R + qt64 - 1) / qt64;
-  const size_t slots = static_cast<size_t>(sh.Hkv) * n_q64 * 64;
+                            float* rowstats, const AttnShape& sh, cudaStream_t s) {
+  const int64_t n_qt = (sh.R + sh.qt - 1) / sh.qt;
+  const size_t slots = static_cast<size_t>(sh.Hkv) * n_qt * 128;
   bwd_prep_kernel<<<grid_for(slots * 32), kThreads, 0, s>>>(
       reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(d_out), lse, rowstats, sh,
-      qt64, n_q64);
+      n_qt);
   return cudaGetLastError();
 }
 

@@ -190,10 +190,8 @@ struct ls_prefix_s {
   const void* v_prefix;
   float* dk_acc;
   float* dv_acc;
-  CUtensorMap tm_k;     // box {64, 1, 128}: forward and dK/dV key tiles
+  CUtensorMap tm_k;     // box {64, 1, 128}: every 128-key tile of the prompt
   CUtensorMap tm_v;
-  CUtensorMap tm_k64;   // box {64, 1, 64}: dQ key steps
-  CUtensorMap tm_v64;
 };
 
 namespace {
@@ -280,8 +278,6 @@ ls_status ls_prefix_prepare(const ls_prefix_desc* d, ls_prefix_t* out, void* str
   h->dv_acc = d->dv_acc;
   st = encode_thd(&h->tm_k, d->k_prefix, d->P, d->Hkv, d->D, 1, 128);
   if (st == LS_OK) st = encode_thd(&h->tm_v, d->v_prefix, d->P, d->Hkv, d->D, 1, 128);
-  if (st == LS_OK) st = encode_thd(&h->tm_k64, d->k_prefix, d->P, d->Hkv, d->D, 1, 64);
-  if (st == LS_OK) st = encode_thd(&h->tm_v64, d->v_prefix, d->P, d->Hkv, d->D, 1, 64);
   if (st != LS_OK) {
     delete h;
     return st;
@@ -350,9 +346,8 @@ ls_status ls_replay_fwd(ls_prefix_t h, int64_t R, const void* q, const void* k_s
 
 size_t ls_replay_bwd_workspace_bytes(ls_prefix_t h, int64_t R) {
   if (check_handle(h) != LS_OK || R < 1) return 0;
-  const int64_t qt64 = 64 / h->shape.g;
-  const int64_t n_q64 = (R + qt64 - 1) / qt64;
-  return align_up(static_cast<size_t>(h->shape.Hkv) * n_q64 * 64 * sizeof(float2), 256);
+  const int64_t n_qt = (R + h->shape.qt - 1) / h->shape.qt;
+  return align_up(static_cast<size_t>(h->shape.Hkv) * n_qt * 256 * sizeof(float), 256);
 }
 
 ls_status ls_replay_bwd(ls_prefix_t h, int64_t R, const void* q, const void* k_suffix,
@@ -380,22 +375,15 @@ ls_status ls_replay_bwd(ls_prefix_t h, int64_t R, const void* q, const void* k_s
   BwdArgs a{};
   a.sh = h->shape;
   a.sh.R = R;
-  a.qt64 = 64 / a.sh.g;
-  a.tm_kp128 = &h->tm_k;
-  a.tm_vp128 = &h->tm_v;
-  a.tm_kp64 = &h->tm_k64;
-  a.tm_vp64 = &h->tm_v64;
+  a.tm_kp = &h->tm_k;
+  a.tm_vp = &h->tm_v;
   const AttnShape& sh = a.sh;
-  st = encode_thd(&a.tm_q64, q, R, sh.Hq, sh.D, sh.g, a.qt64);
-  if (st == LS_OK) st = encode_thd(&a.tm_do64, d_out, R, sh.Hq, sh.D, sh.g, a.qt64);
-  if (st == LS_OK) st = encode_thd(&a.tm_q128, q, R, sh.Hq, sh.D, sh.g, sh.qt);
-  if (st == LS_OK) st = encode_thd(&a.tm_do128, d_out, R, sh.Hq, sh.D, sh.g, sh.qt);
-  if (st == LS_OK) st = encode_thd(&a.tm_ks128, k_suffix, R, sh.Hkv, sh.D, 1, 128);
-  if (st == LS_OK) st = encode_thd(&a.tm_vs128, v_suffix, R, sh.Hkv, sh.D, 1, 128);
-  if (st == LS_OK) st = encode_thd(&a.tm_ks64, k_suffix, R, sh.Hkv, sh.D, 1, 64);
-  if (st == LS_OK) st = encode_thd(&a.tm_vs64, v_suffix, R, sh.Hkv, sh.D, 1, 64);
+  st = encode_thd(&a.tm_q, q, R, sh.Hq, sh.D, sh.g, sh.qt);
+  if (st == LS_OK) st = encode_thd(&a.tm_do, d_out, R, sh.Hq, sh.D, sh.g, sh.qt);
+  if (st == LS_OK) st = encode_thd(&a.tm_ks, k_suffix, R, sh.Hkv, sh.D, 1, 128);
+  if (st == LS_OK) st = encode_thd(&a.tm_vs, v_suffix, R, sh.Hkv, sh.D, 1, 128);
   if (st != LS_OK) return st;
-  float2* rowstats = static_cast<float2*>(workspace);
+  float* rowstats = static_cast<float*>(workspace);
   a.rowstats = rowstats;
   a.dq = static_cast<uint16_t*>(dq);
   a.dk_suf = static_cast<uint16_t*>(dk_suffix);
@@ -408,7 +396,7 @@ ls_status ls_replay_bwd(ls_prefix_t h, int64_t R, const void* q, const void* k_s
   {
     LaunchTimer t(LS_KERNEL_BWD_PREP, s);
     e = launch_bwd_prep(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(d_out), lse,
-                        rowstats, sh, a.qt64, s);
+                        rowstats, sh, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "replay backward prep launch");
   {

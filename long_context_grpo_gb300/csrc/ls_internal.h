@@ -54,27 +54,23 @@ cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t s);
 
 struct BwdArgs {
   AttnShape sh;
-  int qt64;                       // queries per 64-row sub-tile (= 64 / g) used by dK/dV
-  const CUtensorMap* tm_kp128;    // prompt K/V, box {64, 1, 128} (dK/dV key tiles)
-  const CUtensorMap* tm_vp128;
-  const CUtensorMap* tm_kp64;     // prompt K/V, box {64, 1, 64} (dQ key steps)
-  const CUtensorMap* tm_vp64;
-  CUtensorMap tm_q64, tm_do64;    // [R][Hq][D], box {64, g, qt64}
-  CUtensorMap tm_q128, tm_do128;  // [R][Hq][D], box {64, g, qt}
-  CUtensorMap tm_ks128, tm_vs128; // suffix K/V, box {64, 1, 128}
-  CUtensorMap tm_ks64, tm_vs64;   // suffix K/V, box {64, 1, 64}
-  const float2* rowstats;         // [Hkv][n_q64][64] (LSE * log2 e, Delta), packed by sub-tile row
-  uint16_t* dq;                   // bf16 [R, Hq, D]
-  uint16_t* dk_suf;               // bf16 [R, Hkv, D]
+  const CUtensorMap* tm_kp;   // prompt K/V [P][Hkv][D], box {64, 1, 128}
+  const CUtensorMap* tm_vp;
+  CUtensorMap tm_q, tm_do;    // [R][Hq][D], box {64, g, qt}
+  CUtensorMap tm_ks, tm_vs;   // suffix K/V [R][Hkv][D], box {64, 1, 128}
+  const float* rowstats;      // [Hkv][n_qt][256]: LSE log2 e of the tile's 128 rows, then Delta
+  uint16_t* dq;               // bf16 [R, Hq, D]
+  uint16_t* dk_suf;           // bf16 [R, Hkv, D]
   uint16_t* dv_suf;
-  float* dk_acc;                  // fp32 [P, Hkv, D]
+  float* dk_acc;              // fp32 [P, Hkv, D]
   float* dv_acc;
   uint32_t* status;
 };
-// rowstats[(kv, i, r)] for every 64-row sub-tile slot: valid rows get (LSE log2 e, Delta),
-// padding rows and rows past R get (+inf, 0) so their softmax probabilities are exactly 0.
+// Row statistics of every 128-row Q tile slot (kv, i, r), r = (t - i qt) g + h - kv g:
+// valid rows get LSE log2 e and Delta = sum_d dO O; padding rows and rows past R get
+// (+inf, 0) so their softmax probabilities are exactly 0.
 cudaError_t launch_bwd_prep(const uint16_t* o, const uint16_t* d_out, const float* lse,
-                            float2* rowstats, const AttnShape& sh, int qt64, cudaStream_t s);
+                            float* rowstats, const AttnShape& sh, cudaStream_t s);
 cudaError_t launch_attn_bwd_dkdv(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_attn_bwd_dq(const BwdArgs& a, cudaStream_t s);
 
