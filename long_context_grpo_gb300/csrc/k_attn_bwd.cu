@@ -52,13 +52,16 @@ template <int D>
 struct DkdvCfg {
   static constexpr int kBoxes = D / 64;
   static constexpr int kTile = 128 * D * 2;         // K, V, Q or dO tile (128 rows)
-  static constexpr int kNS = (D == 128) ? 2 : 4;    // Q/dO ring stages
-  static constexpr int kStage = 2 * kTile + 1024;   // Q, dO, row stats (LSE2[128], Delta[128])
-  static constexpr int kOffK = 0, kOffV = kTile, kOffStage = 2 * kTile;
-  static constexpr int kOffBar = kOffStage + kNS * kStage;
+  static constexpr int kNQ = 3;                     // Q ring: needed early (S) and late (dK)
+  static constexpr int kNO = 2;                     // dO ring: needed by dP and dV
+  static constexpr int kOffK = 0, kOffV = kTile, kOffQ = 2 * kTile;
+  static constexpr int kOffO = kOffQ + kNQ * kTile;
+  static constexpr int kOffBar = kOffO + kNO * kTile;
   static constexpr int kBarKVFull = 0, kBarKVEmpty = 1, kBarQFull = 2;
-  static constexpr int kBarQEmpty = kBarQFull + kNS;
-  static constexpr int kBarSFull = kBarQEmpty + kNS;
+  static constexpr int kBarQEmpty = kBarQFull + kNQ;
+  static constexpr int kBarOFull = kBarQEmpty + kNQ;
+  static constexpr int kBarOEmpty = kBarOFull + kNO;
+  static constexpr int kBarSFull = kBarOEmpty + kNO;
   static constexpr int kBarSFree = kBarSFull + 1;
   static constexpr int kBarDPFull = kBarSFree + 1;
   static constexpr int kBarPDSFull = kBarDPFull + 1;
@@ -117,21 +120,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_units = sh.Hkv * static_cast<int>((sh.P + 127) / 128 + (sh.R + 127) / 128);
   const int rows_used = sh.g * sh.qt;   // rows of a 128-row tile that TMA fills
 
-  // Padding rows of every Q/dO stage are never written by TMA: zero them once so that
+  // Padding rows of every Q/dO buffer are never written by TMA: zero them once so that
   // they contribute exactly nothing to the sums over rows in dK and dV.
   if (rows_used < 128) {
     const int pad_rows = 128 - rows_used;
-    const int per_buf = C::kBoxes * pad_rows * 8;   // 16-byte chunks per Q or dO buffer
-    for (int idx = threadIdx.x; idx < C::kNS * 2 * per_buf; idx += kThreads) {
-      const int st = idx / (2 * per_buf);
-      int rem = idx - st * 2 * per_buf;
-      const int buf = rem / per_buf;                 // 0 = Q, 1 = dO
-      rem -= buf * per_buf;
+    const int per_buf = C::kBoxes * pad_rows * 8;   // 16-byte chunks per buffer
+    for (int idx = threadIdx.x; idx < (C::kNQ + C::kNO) * per_buf; idx += kThreads) {
+      const int buf = idx / per_buf;                 // Q ring buffers, then dO ring buffers
+      int rem = idx - buf * per_buf;
       const int box = rem / (pad_rows * 8);
       rem -= box * (pad_rows * 8);
       const int row = rows_used + rem / 8, chunk = rem & 7;
-      uint8_t* p = smem + C::kOffStage + st * C::kStage + buf * C::kTile + box * 16384 +
-                   row * 128 + chunk * 16;
+      uint8_t* p = smem + C::kOffQ + buf * C::kTile + box * 16384 + row * 128 + chunk * 16;
       *reinterpret_cast<uint4*>(p) = make_uint4(0u, 0u, 0u, 0u);
     }
     fence_proxy_async_smem();
@@ -140,9 +140,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     abort_flag = 0;
     mbar_init(&bars[C::kBarKVFull], 1);
     mbar_init(&bars[C::kBarKVEmpty], 1);
-    for (int i = 0; i < C::kNS; ++i) {
+    for (int i = 0; i < C::kNQ; ++i) {
       mbar_init(&bars[C::kBarQFull + i], 1);
       mbar_init(&bars[C::kBarQEmpty + i], 1);
+    }
+    for (int i = 0; i < C::kNO; ++i) {
+      mbar_init(&bars[C::kBarOFull + i], 1);
+      mbar_init(&bars[C::kBarOEmpty + i], 1);
     }
     mbar_init(&bars[C::kBarSFull], 1);
     mbar_init(&bars[C::kBarSFree], 256);
@@ -163,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   volatile int* vabort = &abort_flag;
-  const uint32_t q_tx = static_cast<uint32_t>(2 * C::kBoxes * 128 * rows_used + 1024);
+  const uint32_t tile_tx = static_cast<uint32_t>(C::kBoxes * 128 * rows_used);
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -190,27 +194,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         kv_pending = true;
         for (int li = 0; li < w.n && ok; ++li, ++qit) {
           const int i = w.i0 + li;
-          const uint32_t st = qit % C::kNS;
-          if (qit >= static_cast<uint32_t>(C::kNS))
-            ok = mbar_wait(&bars[C::kBarQEmpty + st], ((qit / C::kNS) - 1) & 1u, status, vabort);
+          const uint32_t sq = qit % C::kNQ, so = qit % C::kNO;
+          if (qit >= static_cast<uint32_t>(C::kNQ))
+            ok = mbar_wait(&bars[C::kBarQEmpty + sq], ((qit / C::kNQ) - 1) & 1u, status, vabort);
           if (!ok) break;
-          uint8_t* base = smem + C::kOffStage + st * C::kStage;
-          mbar_arrive_expect_tx(&bars[C::kBarQFull + st], q_tx);
-          for (int b = 0; b < C::kBoxes; ++b) {
-            tma_load_3d(base + b * 16384, &tm_q, &bars[C::kBarQFull + st], 64 * b, w.kv * sh.g,
-                        i * sh.qt);
-            tma_load_3d(base + C::kTile + b * 16384, &tm_do, &bars[C::kBarQFull + st], 64 * b,
-                        w.kv * sh.g, i * sh.qt);
-          }
-          bulk_load(base + 2 * C::kTile, rowstats + (static_cast<int64_t>(w.kv) * n_qt + i) * 256,
-                    1024, &bars[C::kBarQFull + st]);
+          mbar_arrive_expect_tx(&bars[C::kBarQFull + sq], tile_tx);
+          for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_3d(smem + C::kOffQ + sq * C::kTile + b * 16384, &tm_q,
+                        &bars[C::kBarQFull + sq], 64 * b, w.kv * sh.g, i * sh.qt);
+          if (qit >= static_cast<uint32_t>(C::kNO))
+            ok = mbar_wait(&bars[C::kBarOEmpty + so], ((qit / C::kNO) - 1) & 1u, status, vabort);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&bars[C::kBarOFull + so], tile_tx);
+          for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_3d(smem + C::kOffO + so * C::kTile + b * 16384, &tm_do,
+                        &bars[C::kBarOFull + so], 64 * b, w.kv * sh.g, i * sh.qt);
         }
       }
       if (!ok) {
         *vabort = 1;
-        // drain this thread's own copies still in flight (the last kNS issues)
-        for (uint32_t it = qit > static_cast<uint32_t>(C::kNS) ? qit - C::kNS : 0u; it < qit; ++it)
-          mbar_wait_ns(&bars[C::kBarQFull + it % C::kNS], (it / C::kNS) & 1u, 200000000ull);
+        // drain this thread's own copies still in flight (the last issues of each ring)
+        for (uint32_t it = qit > static_cast<uint32_t>(C::kNQ) ? qit - C::kNQ : 0u; it < qit; ++it)
+          mbar_wait_ns(&bars[C::kBarQFull + it % C::kNQ], (it / C::kNQ) & 1u, 200000000ull);
+        for (uint32_t it = qit > static_cast<uint32_t>(C::kNO) ? qit - C::kNO : 0u; it < qit; ++it)
+          mbar_wait_ns(&bars[C::kBarOFull + it % C::kNO], (it / C::kNO) & 1u, 200000000ull);
         if (kv_pending) mbar_wait_ns(&bars[C::kBarKVFull], (uc) & 1u, 200000000ull);
       }
     }
@@ -221,18 +228,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdAcc = idesc_bf16(128, D, false, true);
       const uint64_t dK0 = smem_desc(smem_u32(smem + C::kOffK), 16, 1024);
       const uint64_t dV0 = smem_desc(smem_u32(smem + C::kOffV), 16, 1024);
-      const uint32_t sStage = smem_u32(smem + C::kOffStage);
-      const uint64_t dS0 = smem_desc(sStage, 16, 1024);      // K-major view of a stage
-      const uint64_t dM0 = smem_desc(sStage, 16384, 1024);   // MN-major view of a stage
+      const uint64_t dQk = smem_desc(smem_u32(smem + C::kOffQ), 16, 1024);     // K-major
+      const uint64_t dQm = smem_desc(smem_u32(smem + C::kOffQ), 16384, 1024);  // MN-major
+      const uint64_t dOk = smem_desc(smem_u32(smem + C::kOffO), 16, 1024);
+      const uint64_t dOm = smem_desc(smem_u32(smem + C::kOffO), 16384, 1024);
       uint32_t qit = 0, uc = 0, n_s = 0, n_pds = 0;
       bool ok = true;
-      // S^T = K Q^T for the tile in stage st; waits until the softmax has taken the
+      // S^T = K Q^T for tile number it; waits for its Q and until the softmax has taken the
       // previous S out of TMEM
-      auto issue_s = [&](uint32_t st) -> bool {
+      auto issue_s = [&](uint32_t it) -> bool {
+        const uint32_t sq = it % C::kNQ;
+        if (!mbar_wait(&bars[C::kBarQFull + sq], (it / C::kNQ) & 1u, status, vabort)) return false;
         if (n_s > 0 && !mbar_wait(&bars[C::kBarSFree], (n_s - 1) & 1u, status, vabort))
           return false;
         tc_fence_after();
-        const uint64_t q = dS0 + static_cast<uint64_t>((st * C::kStage) >> 4);
+        const uint64_t q = dQk + static_cast<uint64_t>((sq * C::kTile) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t o = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
@@ -242,18 +252,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++n_s;
         return true;
       };
-      auto issue_dp = [&](uint32_t st) {
-        const uint64_t o_ = dS0 + static_cast<uint64_t>((st * C::kStage + C::kTile) >> 4);
+      auto issue_dp = [&](uint32_t it) -> bool {
+        const uint32_t so = it % C::kNO;
+        if (!mbar_wait(&bars[C::kBarOFull + so], (it / C::kNO) & 1u, status, vabort)) return false;
+        tc_fence_after();
+        const uint64_t o_ = dOk + static_cast<uint64_t>((so * C::kTile) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t o = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
           mma_bf16_ss(tmem + C::kColDP, dV0 + o, o_ + o, kIdS, kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars[C::kBarDPFull]);
+        return true;
       };
-      auto issue_acc = [&](uint32_t st, bool acc) {
-        const uint64_t q = dM0 + static_cast<uint64_t>((st * C::kStage) >> 4);
-        const uint64_t o = q + static_cast<uint64_t>(C::kTile >> 4);
+      auto issue_acc = [&](uint32_t it, bool acc) {
+        const uint64_t q = dQm + static_cast<uint64_t>(((it % C::kNQ) * C::kTile) >> 4);
+        const uint64_t o = dOm + static_cast<uint64_t>(((it % C::kNO) * C::kTile) >> 4);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t ko = static_cast<uint64_t>((kk * 2048) >> 4);
@@ -261,26 +275,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16_ts(tmem + C::kColDV, pc, o + ko, kIdAcc, (acc || kk > 0) ? 1u : 0u);
           mma_bf16_ts(tmem + C::kColDK, pc + 16u, q + ko, kIdAcc, (acc || kk > 0) ? 1u : 0u);
         }
+        mma_commit(&bars[C::kBarQEmpty + it % C::kNQ]);
+        mma_commit(&bars[C::kBarOEmpty + it % C::kNO]);
       };
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
         const KvUnit w = make_kv_unit(u, sh, n_qt);
         ok = mbar_wait(&bars[C::kBarKVFull], uc & 1u, status, vabort);
         if (!ok) break;
-        const uint32_t st0 = qit % C::kNS;
-        ok = mbar_wait(&bars[C::kBarQFull + st0], (qit / C::kNS) & 1u, status, vabort);
-        if (!ok) break;
         tc_fence_after();
-        ok = issue_s(st0);
-        if (!ok) break;
-        issue_dp(st0);
+        ok = issue_s(qit) && issue_dp(qit);
         for (int li = 0; li < w.n && ok; ++li) {
-          const uint32_t st = (qit + li) % C::kNS;
+          const uint32_t it = qit + li;
           const bool more = li + 1 < w.n;
-          const uint32_t st1 = (qit + li + 1) % C::kNS;
           if (more) {
-            ok = mbar_wait(&bars[C::kBarQFull + st1], ((qit + li + 1) / C::kNS) & 1u, status,
-                           vabort);
-            if (ok) ok = issue_s(st1);
+            ok = issue_s(it + 1);
             if (!ok) break;
           }
           ok = mbar_wait(&bars[C::kBarPDSFull], n_pds & 1u, status, vabort);
@@ -291,9 +299,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
           }
           tc_fence_after();
-          issue_acc(st, li > 0);
-          mma_commit(&bars[C::kBarQEmpty + st]);
-          if (more) issue_dp(st1);
+          issue_acc(it, li > 0);
+          if (more) ok = issue_dp(it + 1);
         }
         if (!ok) break;
         qit += w.n;
@@ -317,17 +324,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const KvUnit w = make_kv_unit(u, sh, n_qt);
       const int key = w.key0 + row;
       for (int li = 0; li < w.n; ++li, ++n_tiles) {
-        const uint32_t st = (qit + li) % C::kNS;
+        // row statistics of this Q tile: every thread reads the same 1 KB (L1 broadcast)
+        const float* rs = rowstats + (static_cast<int64_t>(w.kv) * n_qt + w.i0 + li) * 256;
+        const float4* lse4 = reinterpret_cast<const float4*>(rs) + wg * 16;   // rows 64 wg ..
+        const float4* dlt4 = reinterpret_cast<const float4*>(rs + 128) + wg * 16;
         ok = mbar_wait(&bars[C::kBarSFull], n_tiles & 1u, status, vabort);
-        if (ok)   // acquire this stage's row stats (long complete: the MMA waited on it)
-          ok = mbar_wait(&bars[C::kBarQFull + st], ((qit + li) / C::kNS) & 1u, status, vabort);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        const float* rs = reinterpret_cast<const float*>(smem + C::kOffStage + st * C::kStage +
-                                                         2 * C::kTile);
-        const float4* lse4 = reinterpret_cast<const float4*>(rs) + wg * 16;   // rows 64 wg ..
-        const float4* dlt4 = reinterpret_cast<const float4*>(rs + 128) + wg * 16;
         // ---- P^T from S^T (this warpgroup's 64 rows); S leaves TMEM first
         float p[64];
         {
@@ -339,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&bars[C::kBarSFree]);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const float4 l4 = lse4[i];
+            const float4 l4 = __ldg(lse4 + i);
             p[4 * i + 0] = ex2_approx(fmaf(__uint_as_float(sa[4 * i + 0]), c2, -l4.x));
             p[4 * i + 1] = ex2_approx(fmaf(__uint_as_float(sa[4 * i + 1]), c2, -l4.y));
             p[4 * i + 2] = ex2_approx(fmaf(__uint_as_float(sa[4 * i + 2]), c2, -l4.z));
@@ -347,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const float4 l4 = lse4[8 + i];
+            const float4 l4 = __ldg(lse4 + 8 + i);
             p[32 + 4 * i + 0] = ex2_approx(fmaf(__uint_as_float(sb[4 * i + 0]), c2, -l4.x));
             p[32 + 4 * i + 1] = ex2_approx(fmaf(__uint_as_float(sb[4 * i + 1]), c2, -l4.y));
             p[32 + 4 * i + 2] = ex2_approx(fmaf(__uint_as_float(sb[4 * i + 2]), c2, -l4.z));
@@ -378,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t pw[16], dw[16];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const float4 d4 = dlt4[ch * 8 + i];
+            const float4 d4 = __ldg(dlt4 + ch * 8 + i);
             const int c = ch * 32 + 4 * i;
             const float s0 = p[c + 0] * (__uint_as_float(dv[4 * i + 0]) - d4.x);
             const float s1 = p[c + 1] * (__uint_as_float(dv[4 * i + 1]) - d4.y);
@@ -459,13 +463,16 @@ template <int D>
 struct DqCfg {
   static constexpr int kBoxes = D / 64;
   static constexpr int kTile = 128 * D * 2;         // Q, dO, K or V tile (128 rows)
-  static constexpr int kNS = (D == 128) ? 2 : 4;    // K/V ring stages
-  static constexpr int kStage = 2 * kTile;
-  static constexpr int kOffQ = 0, kOffDO = kTile, kOffStage = 2 * kTile;
-  static constexpr int kOffBar = kOffStage + kNS * kStage;
-  static constexpr int kBarQFull = 0, kBarQEmpty = 1, kBarQTmem = 2, kBarKVFull = 3;
-  static constexpr int kBarKVEmpty = kBarKVFull + kNS;
-  static constexpr int kBarSFull = kBarKVEmpty + kNS;
+  static constexpr int kNK = 3;                     // K ring: needed early (S) and late (dQ)
+  static constexpr int kNV = 2;                     // V ring: needed by dP only
+  static constexpr int kOffQ = 0, kOffDO = kTile, kOffK = 2 * kTile;
+  static constexpr int kOffV = kOffK + kNK * kTile;
+  static constexpr int kOffBar = kOffV + kNV * kTile;
+  static constexpr int kBarQFull = 0, kBarQEmpty = 1, kBarQTmem = 2, kBarKFull = 3;
+  static constexpr int kBarKEmpty = kBarKFull + kNK;
+  static constexpr int kBarVFull = kBarKEmpty + kNK;
+  static constexpr int kBarVEmpty = kBarVFull + kNV;
+  static constexpr int kBarSFull = kBarVEmpty + kNV;
   static constexpr int kBarSFree = kBarSFull + 1;
   static constexpr int kBarDPFull = kBarSFree + 1;
   static constexpr int kBarDSFull = kBarDPFull + 1;
@@ -527,9 +534,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[C::kBarQFull], 1);
     mbar_init(&bars[C::kBarQEmpty], 256);
     mbar_init(&bars[C::kBarQTmem], 256);
-    for (int i = 0; i < C::kNS; ++i) {
-      mbar_init(&bars[C::kBarKVFull + i], 1);
-      mbar_init(&bars[C::kBarKVEmpty + i], 1);
+    for (int i = 0; i < C::kNK; ++i) {
+      mbar_init(&bars[C::kBarKFull + i], 1);
+      mbar_init(&bars[C::kBarKEmpty + i], 1);
+    }
+    for (int i = 0; i < C::kNV; ++i) {
+      mbar_init(&bars[C::kBarVFull + i], 1);
+      mbar_init(&bars[C::kBarVEmpty + i], 1);
     }
     mbar_init(&bars[C::kBarSFull], 1);
     mbar_init(&bars[C::kBarSFree], 256);
@@ -575,26 +586,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                       w.kv * sh.g, w.t0);
         }
         for (int j = 0; j < w.n && ok; ++j, ++kit) {
-          const uint32_t st = kit % C::kNS;
-          if (kit >= static_cast<uint32_t>(C::kNS))
-            ok = mbar_wait(&bars[C::kBarKVEmpty + st], ((kit / C::kNS) - 1) & 1u, status, vabort);
-          if (!ok) break;
           const bool pre = j < w.n_pt;
           const int key0 = pre ? 128 * j : 128 * (j - w.n_pt);
-          uint8_t* base = smem + C::kOffStage + st * C::kStage;
-          mbar_arrive_expect_tx(&bars[C::kBarKVFull + st], 2 * C::kTile);
-          for (int b = 0; b < C::kBoxes; ++b) {
-            tma_load_3d(base + b * 16384, pre ? &tm_kp : &tm_ks, &bars[C::kBarKVFull + st],
-                        64 * b, w.kv, key0);
-            tma_load_3d(base + C::kTile + b * 16384, pre ? &tm_vp : &tm_vs,
-                        &bars[C::kBarKVFull + st], 64 * b, w.kv, key0);
-          }
+          const uint32_t sk = kit % C::kNK, sv = kit % C::kNV;
+          if (kit >= static_cast<uint32_t>(C::kNK))
+            ok = mbar_wait(&bars[C::kBarKEmpty + sk], ((kit / C::kNK) - 1) & 1u, status, vabort);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&bars[C::kBarKFull + sk], C::kTile);
+          for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_3d(smem + C::kOffK + sk * C::kTile + b * 16384, pre ? &tm_kp : &tm_ks,
+                        &bars[C::kBarKFull + sk], 64 * b, w.kv, key0);
+          if (kit >= static_cast<uint32_t>(C::kNV))
+            ok = mbar_wait(&bars[C::kBarVEmpty + sv], ((kit / C::kNV) - 1) & 1u, status, vabort);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&bars[C::kBarVFull + sv], C::kTile);
+          for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_3d(smem + C::kOffV + sv * C::kTile + b * 16384, pre ? &tm_vp : &tm_vs,
+                        &bars[C::kBarVFull + sv], 64 * b, w.kv, key0);
         }
       }
       if (!ok) {
         *vabort = 1;
-        for (uint32_t it = kit > static_cast<uint32_t>(C::kNS) ? kit - C::kNS : 0u; it < kit; ++it)
-          mbar_wait_ns(&bars[C::kBarKVFull + it % C::kNS], (it / C::kNS) & 1u, 200000000ull);
+        for (uint32_t it = kit > static_cast<uint32_t>(C::kNK) ? kit - C::kNK : 0u; it < kit; ++it)
+          mbar_wait_ns(&bars[C::kBarKFull + it % C::kNK], (it / C::kNK) & 1u, 200000000ull);
+        for (uint32_t it = kit > static_cast<uint32_t>(C::kNV) ? kit - C::kNV : 0u; it < kit; ++it)
+          mbar_wait_ns(&bars[C::kBarVFull + it % C::kNV], (it / C::kNV) & 1u, 200000000ull);
         mbar_wait_ns(&bars[C::kBarQFull], (uc) & 1u, 200000000ull);
       }
     }
@@ -603,16 +619,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t kIdQ = idesc_bf16(128, D, false, true);
-      const uint32_t sStage = smem_u32(smem + C::kOffStage);
-      const uint64_t dK0 = smem_desc(sStage, 16, 1024);      // K-major view of a stage
-      const uint64_t dM0 = smem_desc(sStage, 16384, 1024);   // MN-major view of a stage
+      const uint64_t dKk = smem_desc(smem_u32(smem + C::kOffK), 16, 1024);      // K-major
+      const uint64_t dKm = smem_desc(smem_u32(smem + C::kOffK), 16384, 1024);   // MN-major
+      const uint64_t dVk = smem_desc(smem_u32(smem + C::kOffV), 16, 1024);
       uint32_t kit = 0, uc = 0, n_s = 0, n_ds = 0;
       bool ok = true;
-      auto issue_s = [&](uint32_t st) -> bool {
+      // S = Q K^T for key step number it; waits for its K and until the softmax has taken
+      // the previous S out of TMEM
+      auto issue_s = [&](uint32_t it) -> bool {
+        const uint32_t sk = it % C::kNK;
+        if (!mbar_wait(&bars[C::kBarKFull + sk], (it / C::kNK) & 1u, status, vabort)) return false;
         if (n_s > 0 && !mbar_wait(&bars[C::kBarSFree], (n_s - 1) & 1u, status, vabort))
           return false;
         tc_fence_after();
-        const uint64_t k = dK0 + static_cast<uint64_t>((st * C::kStage) >> 4);
+        const uint64_t k = dKk + static_cast<uint64_t>((sk * C::kTile) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t o = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
@@ -622,8 +642,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++n_s;
         return true;
       };
-      auto issue_dp = [&](uint32_t st) {
-        const uint64_t v = dK0 + static_cast<uint64_t>((st * C::kStage + C::kTile) >> 4);
+      auto issue_dp = [&](uint32_t it) -> bool {
+        const uint32_t sv = it % C::kNV;
+        if (!mbar_wait(&bars[C::kBarVFull + sv], (it / C::kNV) & 1u, status, vabort)) return false;
+        tc_fence_after();
+        const uint64_t v = dVk + static_cast<uint64_t>((sv * C::kTile) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t o = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
@@ -631,34 +654,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                       kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars[C::kBarDPFull]);
+        mma_commit(&bars[C::kBarVEmpty + sv]);   // V is read by dP only
+        return true;
       };
-      auto issue_dq = [&](uint32_t st, bool acc) {
-        const uint64_t k = dM0 + static_cast<uint64_t>((st * C::kStage) >> 4);
+      auto issue_dq = [&](uint32_t it, bool acc) {
+        const uint32_t sk = it % C::kNK;
+        const uint64_t k = dKm + static_cast<uint64_t>((sk * C::kTile) >> 4);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_bf16_ts(tmem + C::kColDQ, tmem + C::kColDP + packed_col(kk),
                       k + static_cast<uint64_t>((kk * 2048) >> 4), kIdQ,
                       (acc || kk > 0) ? 1u : 0u);
+        mma_commit(&bars[C::kBarKEmpty + sk]);
       };
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
         const QUnit w = make_q_unit(u, sh, n_qt);
         ok = mbar_wait(&bars[C::kBarQTmem], uc & 1u, status, vabort);
         if (!ok) break;
-        const uint32_t st0 = kit % C::kNS;
-        ok = mbar_wait(&bars[C::kBarKVFull + st0], (kit / C::kNS) & 1u, status, vabort);
-        if (!ok) break;
         tc_fence_after();
-        ok = issue_s(st0);
-        if (!ok) break;
-        issue_dp(st0);
+        ok = issue_s(kit) && issue_dp(kit);
         for (int j = 0; j < w.n && ok; ++j) {
-          const uint32_t st = (kit + j) % C::kNS;
+          const uint32_t it = kit + j;
           const bool more = j + 1 < w.n;
-          const uint32_t st1 = (kit + j + 1) % C::kNS;
           if (more) {
-            ok = mbar_wait(&bars[C::kBarKVFull + st1], ((kit + j + 1) / C::kNS) & 1u, status,
-                           vabort);
-            if (ok) ok = issue_s(st1);
+            ok = issue_s(it + 1);
             if (!ok) break;
           }
           ok = mbar_wait(&bars[C::kBarDSFull], n_ds & 1u, status, vabort);
@@ -669,9 +688,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
           }
           tc_fence_after();
-          issue_dq(st, j > 0);
-          mma_commit(&bars[C::kBarKVEmpty + st]);
-          if (more) issue_dp(st1);
+          issue_dq(it, j > 0);
+          if (more) ok = issue_dp(it + 1);
         }
         if (!ok) break;
         kit += w.n;
