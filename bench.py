@@ -275,6 +275,15 @@ class Group:
         pre.finalize(1.0, self.dk_out, self.dv_out)
         pre.close()
 
+    def score(self):
+        """Old/reference-policy scoring of the group: forward replay + token log-probs."""
+        import long_context_grpo_gb300 as ls
+        pre = ls.Prefix(self.kp, self.vp, self.dk_acc, self.dv_acc, Hq=self.w.Hq)
+        for r, Ri in zip(self.resp, self.R):
+            pre.fwd(r["q"], r["ks"], r["vs"], o=self.o[:Ri], lse=self.lse[:Ri])
+            ls.token_logp(r["logits"], r["ids"], logp_out=self.logp[:Ri])
+        pre.close()
+
     def flops(self):
         w = self.w
         return sum(14 * w.D * w.Hq * pairs(w.P, Ri) for Ri in self.R)
@@ -389,6 +398,31 @@ def run_ours(args, w):
                 "peak_source": peak_src + (" sustained bf16" if d["bound"] == "tensor" else " HBM copy")}
     launches = sum(v["launches"] * KERNELS_PER_BRACKET.get(k, 1) for k, v in kernels.items())
 
+    # ---------------- old/reference-policy scoring of the same group (no gradients)
+    score = None
+    if not args.no_score:
+        grp.score()   # untimed
+        torch.cuda.synchronize()
+        ls.timing_read()
+        ls.timing_enable(True)
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        grp.score()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        ls.timing_enable(False)
+        st_k = ls.timing_read()
+        sms = s0.elapsed_time(s1)
+        fwd_flops = sum(4 * w.D * w.Hq * pairs(w.P, Ri) for Ri in grp.R)
+        lp_ms, lp_n = st_k["token_logp"]
+        lp_bytes = sum(Ri * (2 * w.V + 8) for Ri in grp.R)
+        score = {"ms": sms, "fwd_tflops": fwd_flops / (sms / 1e3) / 1e12,
+                 "response_tok_s": sum(grp.R) / (sms / 1e3),
+                 "token_logp": {"launches": lp_n, "avg_ms": lp_ms / max(lp_n, 1),
+                                "achieved_gbs": lp_bytes / (lp_ms / 1e3) / 1e9 if lp_ms > 0 else None,
+                                "frac_hbm": (lp_bytes / (lp_ms / 1e3) / 1e9) / peaks["hbm_gbs"] if lp_ms > 0 else None}}
+
     # ---------------- end to end through the C ABI with host buffers
     e2e = None
     if not args.no_e2e:
@@ -453,6 +487,7 @@ def run_ours(args, w):
                 "clocks": clk,
                 "e2e": e2e,
                 "cpu_baseline": cpu,
+                "scoring": score,
                 "receipt": {"gradient_semantics": "prompt dK/dV exposed (fp32, group-summed), "
                                                   "not propagated",
                             "residency": "prompt K/V resident in HBM for the group",
@@ -474,6 +509,7 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=8)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-score", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("at least 3 warm-up steps")

@@ -165,6 +165,19 @@ ls_status ls_grpo_loss(int64_t R, int64_t V, int32_t G, const void* logits, cons
                        size_t workspace_bytes, void* stream);
 
 /*
+ * ls_token_logp -- token log-probabilities without gradients, for the old- and
+ * reference-policy scoring of the responses from the preserved prompt state (review
+ * section 2-1 step 2; section 4-2 step 4 of the GLM recipe):
+ *     logp_out[t] = x[t, y_t] - log sum_v exp(x[t, v])     (natural log)
+ *   logits device bf16 [R, V]; ids device int32 [R] (an id outside [0, V) sets the device
+ *   status and gives 0); logp_out device fp32 [R] (written).  One read of the logits; the
+ *   row log-sum-exp is combined in fp64 as in ls_grpo_loss (so the values are identical to
+ *   ls_grpo_loss's logp_out).  The attention part of scoring is ls_replay_fwd.
+ */
+ls_status ls_token_logp(int64_t R, int64_t V, const void* logits, const int32_t* ids,
+                        float* logp_out, void* stream);
+
+/*
  * ls_grpo_loss_noalloc -- ls_grpo_loss for callers that cannot allocate device memory.
  * (The reviewed pages have no counterpart: this is a deployment variant of the loss.)
  * Same arguments, semantics and outputs as ls_grpo_loss, without the workspace: the
@@ -225,12 +238,22 @@ typedef enum {
   LS_KERNEL_BWD_DQ = 4,        /* dQ                                              */
   LS_KERNEL_GRPO_LOSS = 5,     /* loss row pass + fixed-order reduction           */
   LS_KERNEL_FINALIZE = 6,      /* prompt-gradient finalization                    */
-  LS_KERNEL_COUNT = 7
+  LS_KERNEL_TOKEN_LOGP = 7,    /* scoring: token log-prob only                    */
+  LS_KERNEL_COUNT = 8
 } ls_kernel_id;
 
 ls_status ls_timing_enable(int enable);
 /* total_ms and launches have room for n >= LS_KERNEL_COUNT entries (host arrays). */
 ls_status ls_timing_read(double* total_ms, int64_t* launches, int n);
+
+/*
+ * Failure-detection self test: enqueues one kernel whose bounded mbarrier wait can never
+ * complete; after limit_ns (0 < limit_ns <= 10 s) it records the same "bounded wait gave
+ * up" bit the replay kernels record, and exits without faulting.  A following
+ * ls_get_device_status() returns LS_ERR_TIMEOUT (and clears the word); the context stays
+ * usable.
+ */
+ls_status ls_debug_wait_timeout(uint64_t limit_ns, void* stream);
 
 const char* ls_status_string(ls_status s);
 

@@ -55,6 +55,7 @@ def _load():
         "ls_grpo_loss_workspace_bytes": (sz, [i64]),
         "ls_grpo_loss": (ctypes.c_int, [i64, i64, i32, vp, vp, vp, ctypes.c_double,
                                         ctypes.c_double, vp, vp, vp, vp, vp, sz, vp]),
+        "ls_token_logp": (ctypes.c_int, [i64, i64, vp, vp, vp, vp]),
         "ls_grpo_loss_noalloc": (ctypes.c_int, [i64, i64, i32, vp, vp, vp, ctypes.c_double,
                                                 ctypes.c_double, vp, vp, vp, vp, vp]),
         "ls_grpo_loss_noalloc_max_rows": (i64, []),
@@ -62,6 +63,7 @@ def _load():
                                                    ctypes.c_int, vp]),
         "ls_get_device_status": (ctypes.c_int, [vp, ctypes.POINTER(ctypes.c_uint32)]),
         "ls_timing_enable": (ctypes.c_int, [ctypes.c_int]),
+        "ls_debug_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, vp]),
         "ls_timing_read": (ctypes.c_int, [ctypes.POINTER(ctypes.c_double),
                                           ctypes.POINTER(ctypes.c_int64), ctypes.c_int]),
         "ls_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -219,7 +221,8 @@ def grpo_loss(logits, ids, logp_old, advantage: float, eps: float, G: int, loss_
     return dlogits, clip_mask, logp_out
 
 
-KERNEL_NAMES = ("zero", "replay_fwd", "bwd_prep", "bwd_dkdv", "bwd_dq", "grpo_loss", "finalize")
+KERNEL_NAMES = ("zero", "replay_fwd", "bwd_prep", "bwd_dkdv", "bwd_dq", "grpo_loss", "finalize",
+                "token_logp")
 
 
 def timing_enable(on: bool = True):
@@ -233,6 +236,17 @@ def timing_read():
     cnt = (ctypes.c_int64 * n)()
     _check(_lib().ls_timing_read(ms, cnt, n), "ls_timing_read")
     return {KERNEL_NAMES[i]: (ms[i], cnt[i]) for i in range(n)}
+
+
+def token_logp(logits, ids, logp_out=None):
+    """Scoring without gradients: fp32 log softmax(logits)[ids] per row."""
+    R, V = logits.shape
+    logp_out = torch.empty((R,), dtype=torch.float32, device=logits.device) if logp_out is None else logp_out
+    _check(_lib().ls_token_logp(R, V, _ptr(logits, "logits", torch.bfloat16, (R, V)),
+                                _ptr(ids, "ids", torch.int32, (R,)),
+                                _ptr(logp_out, "logp_out", torch.float32, (R,)), _stream()),
+           "ls_token_logp")
+    return logp_out
 
 
 def device_status():

@@ -6,6 +6,7 @@
 //                      backward dS = P * (dP - Delta), packed with LSE by 128-row Q tile
 // All use 128-bit accesses on a grid sized to the SM count.
 #include "ls_internal.h"
+#include "ptx.cuh"
 
 namespace ls {
 namespace {
@@ -97,6 +98,18 @@ __global__ void __launch_bounds__(kThreads) bwd_prep_kernel(const uint4* o, cons
   }
 }
 
+// Failure-detection self test: one thread waits on an mbarrier that nothing arrives at,
+// bounded by limit_ns, then records DEV_WAIT_TIMEOUT exactly as the replay kernels do when
+// a wait gives up, and exits; the context stays usable.
+__global__ void wait_timeout_kernel(uint64_t limit_ns, uint32_t* status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    if (!mbar_wait_ns(&bar, 0u, limit_ns)) set_device_status(status, DEV_WAIT_TIMEOUT);
+  }
+}
+
 unsigned grid_for(size_t work_items) {
   const size_t per_block = kThreads;
   size_t blocks = (work_items + per_block - 1) / per_block;
@@ -130,6 +143,11 @@ cudaError_t launch_finalize(const float* acc, void* out, size_t n, float scale, 
 cudaError_t launch_scale_inplace(float* acc, size_t n, float scale, cudaStream_t s) {
   const size_t n4 = n / 4;
   scale_kernel<<<grid_for(n4), kThreads, 0, s>>>(reinterpret_cast<float4*>(acc), n4, scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_timeout(uint64_t limit_ns, uint32_t* status, cudaStream_t s) {
+  wait_timeout_kernel<<<1, 32, 0, s>>>(limit_ns, status);
   return cudaGetLastError();
 }
 

@@ -11,6 +11,8 @@
 //           is written as zeros without re-reading.
 // K6 loss_reduce: one CTA sums the per-row loss terms in a fixed order (deterministic)
 //           and adds the total into the fp64 loss accumulator.
+// The scoring variant (old/reference-policy log-probs, review section 2-1 step 2) runs
+// pass 1 and the log-prob only.
 #include <cuda_bf16.h>
 
 #include "ls_internal.h"
@@ -47,7 +49,9 @@ __device__ __forceinline__ void merge_ms(float& m, double& s, float m2, double s
   }
 }
 
-template <bool kVec>
+// kScore: log-prob only (old/reference-policy scoring): pass 1 and logp, no loss, no
+// dlogits, no second read of the row.
+template <bool kVec, bool kScore>
 __global__ void __launch_bounds__(kThreads) grpo_loss_rows(LossArgs a) {
   __shared__ float sh_m[kThreads / 32];
   __shared__ double sh_s[kThreads / 32];
@@ -125,37 +129,49 @@ __global__ void __launch_bounds__(kThreads) grpo_loss_rows(LossArgs a) {
       double S = sh_s[0];
       for (int w = 1; w < kThreads / 32; ++w) merge_ms(M, S, sh_m[w], sh_s[w]);
       const int32_t y = a.ids[row];
-      const double GR = static_cast<double>(a.G) * static_cast<double>(a.R);
-      double term = 0.0, g = 0.0, lse = 0.0, logp = 0.0;
-      uint8_t clipped = 0;
-      if (y < 0 || y >= V) {
-        set_device_status(a.status, DEV_BAD_INDEX);
-        logp = 0.0;
-        lse = 0.0;
+      if constexpr (kScore) {
+        double lp = 0.0;
+        if (y < 0 || y >= V) {
+          set_device_status(a.status, DEV_BAD_INDEX);
+        } else {
+          const double lse = (static_cast<double>(M) + log2(S)) * kLn2;
+          lp = static_cast<double>(__uint_as_float(static_cast<uint32_t>(xr[y]) << 16)) - lse;
+        }
+        a.logp_out[row] = static_cast<float>(lp);
       } else {
-        // lse in natural log: (M + log2 S) * ln 2
-        lse = (static_cast<double>(M) + log2(S)) * kLn2;
-        const double xy = static_cast<double>(__uint_as_float(static_cast<uint32_t>(xr[y]) << 16));
-        logp = xy - lse;
-        const double rho = exp(logp - static_cast<double>(a.logp_old[row]));
-        const double A = a.A;
-        const double clo = 1.0 - a.eps, chi = 1.0 + a.eps;
-        const double rclip = rho < clo ? clo : (rho > chi ? chi : rho);
-        const double unclipped_val = rho * A;
-        const double clipped_val = rclip * A;
-        clipped = (clipped_val < unclipped_val) ? 1 : 0;
-        const double surr = clipped ? clipped_val : unclipped_val;
-        term = -surr / GR;
-        g = clipped ? 0.0 : -A * rho / GR;
+        const double GR = static_cast<double>(a.G) * static_cast<double>(a.R);
+        double term = 0.0, g = 0.0, lse = 0.0, logp = 0.0;
+        uint8_t clipped = 0;
+        if (y < 0 || y >= V) {
+          set_device_status(a.status, DEV_BAD_INDEX);
+          logp = 0.0;
+          lse = 0.0;
+        } else {
+          // lse in natural log: (M + log2 S) * ln 2
+          lse = (static_cast<double>(M) + log2(S)) * kLn2;
+          const double xy = static_cast<double>(__uint_as_float(static_cast<uint32_t>(xr[y]) << 16));
+          logp = xy - lse;
+          const double rho = exp(logp - static_cast<double>(a.logp_old[row]));
+          const double A = a.A;
+          const double clo = 1.0 - a.eps, chi = 1.0 + a.eps;
+          const double rclip = rho < clo ? clo : (rho > chi ? chi : rho);
+          const double unclipped_val = rho * A;
+          const double clipped_val = rclip * A;
+          clipped = (clipped_val < unclipped_val) ? 1 : 0;
+          const double surr = clipped ? clipped_val : unclipped_val;
+          term = -surr / GR;
+          g = clipped ? 0.0 : -A * rho / GR;
+        }
+        a.row_terms[row] = term;
+        a.clip_mask[row] = clipped;
+        if (a.logp_out != nullptr) a.logp_out[row] = static_cast<float>(logp);
+        sh_g = static_cast<float>(g);
+        sh_lse2 = static_cast<float>(lse / kLn2);    // lse in log2 units
+        sh_y = (y < 0 || y >= V) ? -1 : y;
       }
-      a.row_terms[row] = term;
-      a.clip_mask[row] = clipped;
-      if (a.logp_out != nullptr) a.logp_out[row] = static_cast<float>(logp);
-      sh_g = static_cast<float>(g);
-      sh_lse2 = static_cast<float>(lse / kLn2);    // lse in log2 units
-      sh_y = (y < 0 || y >= V) ? -1 : y;
     }
     __syncthreads();
+    if constexpr (kScore) continue;
     const float g = sh_g, lse2 = sh_lse2;
     const int y = sh_y;
 
@@ -239,12 +255,23 @@ cudaError_t launch_grpo_loss(const LossArgs& a, cudaStream_t s) {
   int64_t grid = static_cast<int64_t>(num_sms()) * 4;
   if (grid > a.R) grid = a.R;
   if (vec)
-    grpo_loss_rows<true><<<static_cast<unsigned>(grid), kThreads, 0, s>>>(a);
+    grpo_loss_rows<true, false><<<static_cast<unsigned>(grid), kThreads, 0, s>>>(a);
   else
-    grpo_loss_rows<false><<<static_cast<unsigned>(grid), kThreads, 0, s>>>(a);
+    grpo_loss_rows<false, false><<<static_cast<unsigned>(grid), kThreads, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   loss_reduce<<<1, kReduceThreads, 0, s>>>(a.row_terms, a.R, a.loss_accum);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_token_logp(const LossArgs& a, cudaStream_t s) {
+  const bool vec = (a.V % 8 == 0) && (reinterpret_cast<uintptr_t>(a.logits) % 16 == 0);
+  int64_t grid = static_cast<int64_t>(num_sms()) * 4;
+  if (grid > a.R) grid = a.R;
+  if (vec)
+    grpo_loss_rows<true, true><<<static_cast<unsigned>(grid), kThreads, 0, s>>>(a);
+  else
+    grpo_loss_rows<false, true><<<static_cast<unsigned>(grid), kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -459,6 +459,32 @@ ls_status ls_grpo_loss(int64_t R, int64_t V, int32_t G, const void* logits, cons
   return e == cudaSuccess ? LS_OK : cuda_fail(e, "grpo loss launch");
 }
 
+ls_status ls_token_logp(int64_t R, int64_t V, const void* logits, const int32_t* ids,
+                        float* logp_out, void* stream) {
+  if (logits == nullptr || ids == nullptr || logp_out == nullptr) return LS_ERR_INVALID_ARGUMENT;
+  if (R < 1 || V < 1) return LS_ERR_INVALID_ARGUMENT;
+  if (R >= (int64_t(1) << 31) || V >= (int64_t(1) << 31)) return LS_ERR_UNSUPPORTED;
+  if (!aligned_n(logits, 2) || !aligned_n(ids, 4) || !aligned_n(logp_out, 4))
+    return LS_ERR_MISALIGNED;
+  uint32_t* status = nullptr;
+  ls_status st = enter(nullptr, stream, &status);
+  if (st != LS_OK) return st;
+  LossArgs a{};
+  a.R = R;
+  a.V = V;
+  a.G = 1;
+  a.logits = static_cast<const uint16_t*>(logits);
+  a.ids = ids;
+  a.logp_out = logp_out;
+  a.status = status;
+  cudaError_t e;
+  {
+    LaunchTimer t(LS_KERNEL_TOKEN_LOGP, static_cast<cudaStream_t>(stream));
+    e = launch_token_logp(a, static_cast<cudaStream_t>(stream));
+  }
+  return e == cudaSuccess ? LS_OK : cuda_fail(e, "token log-prob launch");
+}
+
 ls_status ls_prefix_grad_finalize(ls_prefix_t h, float scale, void* dk_out, void* dv_out,
                                   int out_is_fp32, int reset_acc, void* stream) {
   ls_status st = check_handle(h);
@@ -484,6 +510,15 @@ ls_status ls_prefix_grad_finalize(ls_prefix_t h, float scale, void* dk_out, void
       e = launch_finalize(h->dv_acc, dv_out, n, scale, out_is_fp32 ? 1 : 0, reset_acc ? 1 : 0, s);
   }
   return e == cudaSuccess ? LS_OK : cuda_fail(e, "finalize launch");
+}
+
+ls_status ls_debug_wait_timeout(uint64_t limit_ns, void* stream) {
+  if (limit_ns == 0 || limit_ns > 10000000000ull) return LS_ERR_INVALID_ARGUMENT;
+  uint32_t* status = nullptr;
+  ls_status st = enter(nullptr, stream, &status);
+  if (st != LS_OK) return st;
+  cudaError_t e = launch_wait_timeout(limit_ns, status, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? LS_OK : cuda_fail(e, "wait-timeout self test launch");
 }
 
 ls_status ls_timing_enable(int enable) {

@@ -25,11 +25,14 @@ struct LossArgs {
   uint32_t* status;
 };
 cudaError_t launch_grpo_loss(const LossArgs& a, cudaStream_t s);
+// logp_out[t] = x_y - log sum_v exp(x_v) only (uses R, V, logits, ids, logp_out, status)
+cudaError_t launch_token_logp(const LossArgs& a, cudaStream_t s);
 
 // ----- elementwise helpers (k_elementwise.cu)
 cudaError_t launch_zero_f32(float* p, size_t n, cudaStream_t s);
 cudaError_t launch_finalize(const float* acc, void* out, size_t n, float scale, int out_fp32,
                             int reset, cudaStream_t s);
+cudaError_t launch_wait_timeout(uint64_t limit_ns, uint32_t* status, cudaStream_t s);
 cudaError_t launch_scale_inplace(float* acc, size_t n, float scale, cudaStream_t s);
 
 // ----- attention (k_attn_fwd.cu, k_attn_bwd.cu)
