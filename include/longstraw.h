@@ -128,7 +128,7 @@ size_t ls_replay_bwd_workspace_bytes(ls_prefix_t h, int64_t R);
  *     dv_acc  += P^T dO    (prompt keys)   fp32, the handle's accumulator
  * kv-head gradients sum over the g query heads of the group.  Inputs q, k_suffix,
  * v_suffix, o (bf16 THD) and lse (fp32 [R, Hq]) are the ones given to / produced by
- * ls_replay_fwd for this response; d_out is bf16 THD [R, Hq].
+ * ls_replay_fwd for this response; d_out is bf16 THD [R, Hq, D].
  * The prompt accumulators are read-modified-written by exactly one CTA per tile, in
  * stream order with other calls on the handle: no atomics, bitwise deterministic.
  * workspace: device, >= ls_replay_bwd_workspace_bytes(h, R) bytes, 16-byte aligned.
