@@ -156,8 +156,10 @@ size_t ls_grpo_loss_workspace_bytes(int64_t R);
  *   loss_accum device double (accumulated, not cleared); dlogits device bf16 [R, V]
  *   clip_mask device uint8 [R]; logp_out device fp32 [R] (may be NULL)
  *   workspace device, >= ls_grpo_loss_workspace_bytes(R) bytes, 16-byte aligned.
- * The token chain (lse combine, logp, rho, the clip decision, g, the loss terms) runs in
- * fp64; the loss reduction is a fixed-order tree (deterministic).
+ * Precision: the row sums of exp are compensated fp32 sums; lse, logp and the loss terms
+ * are fp64; the clip decision and g use rho evaluated in fp32 from the fp64 log-ratio
+ * (relative error ~2e-7, so the mask equals an exact evaluation except for rho within
+ * ~1e-6 of 1 +- eps).  The loss reduction is a fixed-order tree (deterministic).
  */
 ls_status ls_grpo_loss(int64_t R, int64_t V, int32_t G, const void* logits, const int32_t* ids,
                        const float* logp_old, double advantage, double eps, double* loss_accum,
