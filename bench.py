@@ -284,6 +284,66 @@ class Group:
             ls.token_logp(r["logits"], r["ids"], logp_out=self.logp[:Ri])
         pre.close()
 
+    def block_replay(self, block, stream):
+        """Blockwise suffix replay of the group's longest response (fwd of every block, then
+        bwd of every block in reverse) against the whole-response replay of the same rows;
+        both timed with CUDA events on `stream`, after one untimed run each."""
+        import torch
+        import long_context_grpo_gb300 as ls
+        w = self.w
+        i = max(range(len(self.R)), key=lambda k: self.R[k])
+        R, r = self.R[i], self.resp[i]
+        P0, dev = w.P, self.kp.device
+        kbuf = torch.empty((P0 + R, w.Hkv, w.D), dtype=torch.bfloat16, device=dev)
+        vbuf = torch.empty_like(kbuf)
+        kbuf[:P0] = self.kp
+        kbuf[P0:] = r["ks"]
+        vbuf[:P0] = self.vp
+        vbuf[P0:] = r["vs"]
+        dk = torch.empty(kbuf.shape, dtype=torch.float32, device=dev)
+        dv = torch.empty_like(dk)
+        spans = [(t0, min(R, t0 + block)) for t0 in range(0, R, block)]
+        q, do = r["q"], r["do"]
+        o, lse, dq = self.o[:R], self.lse[:R], self.dq[:R]
+
+        def blocks(pre):
+            for t0, t1 in spans:
+                pre.block_fwd(P0 + t0, q[t0:t1], o[t0:t1], lse[t0:t1])
+            for t0, t1 in reversed(spans):
+                pre.block_bwd(P0 + t0, q[t0:t1], o[t0:t1], lse[t0:t1], do[t0:t1], dq[t0:t1],
+                              workspace=self.bws)
+
+        def whole(pre):
+            pre.fwd(q, r["ks"], r["vs"], o=o, lse=lse)
+            pre.bwd(q, r["ks"], r["vs"], o, lse, do, dq=dq, dk_suffix=self.dks[:R],
+                    dv_suffix=self.dvs[:R], workspace=self.bws)
+
+        def timed(fn, pre):
+            fn(pre)
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn(pre)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1)
+
+        pb = ls.Prefix(kbuf, vbuf, dk, dv, Hq=w.Hq)
+        ms_b = timed(blocks, pb)
+        pb.close()
+        pw = ls.Prefix(self.kp, self.vp, self.dk_acc, self.dv_acc, Hq=w.Hq)
+        ms_w = timed(whole, pw)
+        pw.close()
+        del kbuf, vbuf, dk, dv
+        fl = 14 * w.D * w.Hq * pairs(P0, R)
+        act = lambda n: n * w.Hq * (4 * w.D * 2 + 4)   # q, o, dO, dq (bf16) and lse per row
+        return {"response_tokens": R, "block": block, "blocks": len(spans),
+                "ms": ms_b, "tflops": fl / (ms_b / 1e3) / 1e12,
+                "whole_response_ms": ms_w, "whole_response_tflops": fl / (ms_w / 1e3) / 1e12,
+                "attention_activation_bytes_per_block": act(min(block, R)),
+                "attention_activation_bytes_whole": act(R)}
+
     def flops(self):
         w = self.w
         return sum(14 * w.D * w.Hq * pairs(w.P, Ri) for Ri in self.R)
@@ -423,6 +483,11 @@ def run_ours(args, w):
                                 "achieved_gbs": lp_bytes / (lp_ms / 1e3) / 1e9 if lp_ms > 0 else None,
                                 "frac_hbm": (lp_bytes / (lp_ms / 1e3) / 1e9) / peaks["hbm_gbs"] if lp_ms > 0 else None}}
 
+    # ---------------- blockwise suffix replay of the longest response
+    blk = None
+    if args.block > 0 and rank == 0:
+        blk = grp.block_replay(args.block, stream)
+
     # ---------------- end to end through the C ABI with host buffers
     e2e = None
     if not args.no_e2e:
@@ -488,6 +553,7 @@ def run_ours(args, w):
                 "e2e": e2e,
                 "cpu_baseline": cpu,
                 "scoring": score,
+                "block_replay": blk,
                 "receipt": {"gradient_semantics": "prompt dK/dV exposed (fp32, group-summed), "
                                                   "not propagated",
                             "residency": "prompt K/V resident in HBM for the group",
@@ -510,6 +576,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-score", action="store_true")
+    ap.add_argument("--block", type=int, default=4096,
+                    help="block length of the blockwise-replay measurement (0: skip it)")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("at least 3 warm-up steps")

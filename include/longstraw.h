@@ -138,6 +138,38 @@ ls_status ls_replay_bwd(ls_prefix_t h, int64_t R, const void* q, const void* k_s
                         const void* d_out, void* dq, void* dk_suffix, void* dv_suffix,
                         void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Blockwise suffix replay (review section 3-2 (4), "Blockwise suffix replay": a response is
+ * replayed block by block instead of as one graph, which bounds the response's activation
+ * peak; attention state has to carry across block boundaries exactly).
+ *
+ * Layout: the handle's K/V buffers hold [prompt; response] -- the prompt keys in rows
+ * 0 .. P0-1 and the response's keys and values in rows P0 .. P0+R_total-1, written by the
+ * caller before the block that produces them is replayed; the handle is prepared with
+ * P = P0 + R_total (or more).  A block of R rows that starts at response token t0 calls with
+ * prefix_len = P0 + t0: its queries see the prefix rows 0 .. prefix_len-1 (prompt and
+ * earlier blocks) and, causally, the block's own rows prefix_len .. prefix_len+R-1.
+ *
+ * ls_block_replay_fwd -- O and lse of the block, exactly as ls_replay_fwd would give them
+ * for these rows with prompt = rows 0 .. prefix_len-1 and suffix = the block's own rows.
+ *   q device bf16 THD [R, Hq, D]; o device bf16 THD [R, Hq, D] (written);
+ *   lse device fp32 [R, Hq] (written).  1 <= prefix_len, prefix_len + R <= P.
+ *
+ * ls_block_replay_bwd -- the block's dq (bf16 THD [R, Hq, D], written) and the key/value
+ * gradients of every row it sees: rows 0 .. prefix_len+R-1 of dk_acc/dv_acc get
+ * += s dS^T Q and += P^T dO.  After the last block the response rows of the accumulators
+ * hold the complete gradient of the response's keys and values (every later block has
+ * added its part), and the prompt rows the prompt's part; read them out with
+ * ls_prefix_grad_finalize_rows.  Inputs as ls_replay_bwd; workspace as
+ * ls_replay_bwd_workspace_bytes(h, R).  Accumulation is atomic-free and deterministic, as
+ * for the prompt in ls_replay_bwd.
+ */
+ls_status ls_block_replay_fwd(ls_prefix_t h, int64_t prefix_len, int64_t R, const void* q,
+                              void* o, float* lse, void* stream);
+ls_status ls_block_replay_bwd(ls_prefix_t h, int64_t prefix_len, int64_t R, const void* q,
+                              const void* o, const float* lse, const void* d_out, void* dq,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
 /* Bytes of device workspace ls_grpo_loss needs for R token rows. */
 size_t ls_grpo_loss_workspace_bytes(int64_t R);
 
@@ -217,6 +249,17 @@ int64_t ls_grpo_loss_noalloc_max_rows(void);
  */
 ls_status ls_prefix_grad_finalize(ls_prefix_t h, float scale, void* dk_out, void* dv_out,
                                   int out_is_fp32, int reset_acc, void* stream);
+
+/*
+ * ls_prefix_grad_finalize_rows -- ls_prefix_grad_finalize over accumulator rows
+ * row0 .. row0+nrows-1 only (0 <= row0, row0 + nrows <= P); dk_out, dv_out [nrows, Hkv, D].
+ * Used to take a response's key/value gradients out of the response rows after blockwise
+ * replay (with reset_acc so the rows can hold the next response) and the prompt rows at
+ * the end of the group.
+ */
+ls_status ls_prefix_grad_finalize_rows(ls_prefix_t h, int64_t row0, int64_t nrows, float scale,
+                                       void* dk_out, void* dv_out, int out_is_fp32,
+                                       int reset_acc, void* stream);
 
 /*
  * Read (and clear) the device status word of the current device: synchronises `stream`,

@@ -61,6 +61,10 @@ def _load():
         "ls_grpo_loss_noalloc_max_rows": (i64, []),
         "ls_prefix_grad_finalize": (ctypes.c_int, [vp, ctypes.c_float, vp, vp, ctypes.c_int,
                                                    ctypes.c_int, vp]),
+        "ls_prefix_grad_finalize_rows": (ctypes.c_int, [vp, i64, i64, ctypes.c_float, vp, vp,
+                                                        ctypes.c_int, ctypes.c_int, vp]),
+        "ls_block_replay_fwd": (ctypes.c_int, [vp, i64, i64, vp, vp, vp, vp]),
+        "ls_block_replay_bwd": (ctypes.c_int, [vp, i64, i64, vp, vp, vp, vp, vp, vp, sz, vp]),
         "ls_get_device_status": (ctypes.c_int, [vp, ctypes.POINTER(ctypes.c_uint32)]),
         "ls_timing_enable": (ctypes.c_int, [ctypes.c_int]),
         "ls_debug_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, vp]),
@@ -185,6 +189,50 @@ class Prefix:
             _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream()),
             "ls_replay_bwd")
         return dq, dk_suffix, dv_suffix
+
+    def block_fwd(self, prefix_len: int, q, o=None, lse=None):
+        """Blockwise replay forward: the block's keys/values are rows prefix_len .. of the
+        handle's K/V buffers; its queries see rows 0 .. prefix_len-1 and, causally, its own."""
+        R = q.shape[0]
+        if o is None:
+            o = torch.empty_like(q)
+        if lse is None:
+            lse = torch.empty((R, self.Hq), dtype=torch.float32, device=q.device)
+        _check(_lib().ls_block_replay_fwd(
+            self._h, prefix_len, R,
+            _ptr(q, "q", torch.bfloat16, (R, self.Hq, self.D)),
+            _ptr(o, "o", torch.bfloat16, (R, self.Hq, self.D)),
+            _ptr(lse, "lse", torch.float32, (R, self.Hq)), _stream()), "ls_block_replay_fwd")
+        return o, lse
+
+    def block_bwd(self, prefix_len: int, q, o, lse, d_out, dq=None, workspace=None):
+        """Blockwise replay backward: dq of the block; key/value gradients of rows
+        0 .. prefix_len+R-1 added into the accumulators."""
+        R = q.shape[0]
+        dq = torch.empty_like(q) if dq is None else dq
+        need = self.bwd_workspace_bytes(R)
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+        _check(_lib().ls_block_replay_bwd(
+            self._h, prefix_len, R,
+            _ptr(q, "q", torch.bfloat16, (R, self.Hq, self.D)),
+            _ptr(o, "o", torch.bfloat16, (R, self.Hq, self.D)),
+            _ptr(lse, "lse", torch.float32, (R, self.Hq)),
+            _ptr(d_out, "d_out", torch.bfloat16, (R, self.Hq, self.D)),
+            _ptr(dq, "dq", torch.bfloat16, (R, self.Hq, self.D)),
+            _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream()),
+            "ls_block_replay_bwd")
+        return dq
+
+    def finalize_rows(self, row0: int, nrows: int, scale: float = 1.0, dk_out=None, dv_out=None,
+                      out_fp32=False, reset=False):
+        shp = (nrows, self.Hkv, self.D)
+        dt = torch.float32 if out_fp32 else torch.bfloat16
+        _check(_lib().ls_prefix_grad_finalize_rows(
+            self._h, row0, nrows, scale, _ptr(dk_out, "dk_out", dt, shp),
+            _ptr(dv_out, "dv_out", dt, shp), 1 if out_fp32 else 0, 1 if reset else 0, _stream()),
+            "ls_prefix_grad_finalize_rows")
+        return dk_out, dv_out
 
     def finalize(self, scale: float = 1.0, dk_out=None, dv_out=None, out_fp32=False, reset=False):
         shp = (self.P, self.Hkv, self.D)

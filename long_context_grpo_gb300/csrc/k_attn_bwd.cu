@@ -13,7 +13,8 @@
 //   dP^T = V dO^T into TMEM, the softmax turns them into bf16 P^T and dS^T, and
 //   dV += P^T dO, dK += dS^T Q accumulate in TMEM (tcgen05.mma with A from TMEM).  The
 //   epilogue adds a prompt tile into the fp32 accumulators (read-modify-write by the one CTA
-//   that owns the tile: no atomics, stream-ordered across calls) or stores a suffix tile.
+//   that owns the tile: no atomics, stream-ordered across calls) or stores a suffix tile
+//   (in block replay the suffix tile is added into the accumulators too, at rows P + key).
 // K4 attn_bwd_dq (query-tile outer): a work unit is one 128-row Q tile; it sweeps 128-key
 //   steps over the prompt and the causal suffix, recomputing S and dP and accumulating
 //   dQ += dS K in TMEM.  Splitting dQ from dK/dV costs recomputing S and dP but removes every
@@ -106,7 +107,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const __grid_constant__ CUtensorMap tm_do, const AttnShape sh,
                          const float* __restrict__ rowstats, float* __restrict__ dk_acc,
                          float* __restrict__ dv_acc, uint16_t* __restrict__ dk_suf,
-                         uint16_t* __restrict__ dv_suf, uint32_t* status) {
+                         uint16_t* __restrict__ dv_suf, const int suffix_to_acc,
+                         uint32_t* status) {
   using C = DkdvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -411,14 +413,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t col = wg == 0 ? C::kColDV : C::kColDK;
       const float mul = wg == 0 ? 1.0f : sh.scale;
       const int64_t off = (static_cast<int64_t>(key) * sh.Hkv + w.kv) * D;
+      // fp32 accumulation: prompt keys, and suffix keys in block replay (rows P + key)
+      const bool to_acc = w.prompt || suffix_to_acc != 0;
+      const int64_t off_acc = w.prompt ? off : ((sh.P + key) * sh.Hkv + w.kv) * D;
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t v[32];
         tmem_ld32(lane_base + col + cc * 32, v);
         tmem_ld_wait();
         if (valid) {
-          if (w.prompt) {
-            float4* dst = reinterpret_cast<float4*>((wg == 0 ? dv_acc : dk_acc) + off + cc * 32);
+          if (to_acc) {
+            float4* dst = reinterpret_cast<float4*>((wg == 0 ? dv_acc : dk_acc) + off_acc + cc * 32);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               float4 a = dst[i];
@@ -858,7 +863,7 @@ cudaError_t launch_dkdv_d(const BwdArgs& a, cudaStream_t s) {
   if (n_units < grid) grid = static_cast<int>(n_units);
   attn_bwd_dkdv_kernel<D><<<grid, kThreads, C::kSmem, s>>>(
       *a.tm_kp, *a.tm_vp, a.tm_ks, a.tm_vs, a.tm_q, a.tm_do, a.sh, a.rowstats, a.dk_acc,
-      a.dv_acc, a.dk_suf, a.dv_suf, a.status);
+      a.dv_acc, a.dk_suf, a.dv_suf, a.suffix_to_acc, a.status);
   return cudaGetLastError();
 }
 

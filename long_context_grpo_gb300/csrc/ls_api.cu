@@ -213,6 +213,142 @@ ls_status enter(ls_prefix_t h, void* stream, uint32_t** status) {
   return status_ptr(dev, status);
 }
 
+// Rows [row0, ...) of a prefix-shaped bf16 [P, Hkv, D] buffer.
+const void* block_rows(ls_prefix_t h, const void* base, int64_t row0) {
+  return static_cast<const uint16_t*>(base) + row0 * h->shape.Hkv * h->shape.D;
+}
+
+// Replay forward of R suffix rows against the first P_eff rows of the handle's prefix.
+ls_status replay_fwd_impl(ls_prefix_t h, int64_t P_eff, int64_t R, const void* q,
+                          const void* k_suffix, const void* v_suffix, void* o, float* lse,
+                          void* stream) {
+  if (q == nullptr || k_suffix == nullptr || v_suffix == nullptr || o == nullptr ||
+      lse == nullptr)
+    return LS_ERR_INVALID_ARGUMENT;
+  if (R < 1) return LS_ERR_INVALID_ARGUMENT;
+  if (R >= (int64_t(1) << 31)) return LS_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_suffix) || !aligned16(v_suffix) || !aligned16(o) ||
+      !aligned_n(lse, 4))
+    return LS_ERR_MISALIGNED;
+  uint32_t* status = nullptr;
+  ls_status st = enter(h, stream, &status);
+  if (st != LS_OK) return st;
+
+  FwdArgs a{};
+  a.sh = h->shape;
+  a.sh.P = P_eff;
+  a.sh.R = R;
+  a.tm_kp = &h->tm_k;
+  a.tm_vp = &h->tm_v;
+  const AttnShape& sh = a.sh;
+  st = encode_thd(&a.tm_q, q, R, sh.Hq, sh.D, sh.g, sh.qt);
+  if (st == LS_OK) st = encode_thd(&a.tm_ks, k_suffix, R, sh.Hkv, sh.D, 1, 128);
+  if (st == LS_OK) st = encode_thd(&a.tm_vs, v_suffix, R, sh.Hkv, sh.D, 1, 128);
+  if (st != LS_OK) return st;
+  a.o = static_cast<uint16_t*>(o);
+  a.lse = lse;
+  a.status = status;
+  cudaError_t e;
+  {
+    LaunchTimer t(LS_KERNEL_REPLAY_FWD, static_cast<cudaStream_t>(stream));
+    e = launch_attn_fwd(a, static_cast<cudaStream_t>(stream));
+  }
+  return e == cudaSuccess ? LS_OK : cuda_fail(e, "replay forward launch");
+}
+
+// Replay backward against the first P_eff prefix rows.  suffix_to_acc: the suffix keys'
+// gradients go into the accumulators at rows P_eff + key (dk/dv_suffix unused).
+ls_status replay_bwd_impl(ls_prefix_t h, int64_t P_eff, int64_t R, const void* q,
+                          const void* k_suffix, const void* v_suffix, const void* o,
+                          const float* lse, const void* d_out, void* dq, void* dk_suffix,
+                          void* dv_suffix, int suffix_to_acc, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  if (q == nullptr || k_suffix == nullptr || v_suffix == nullptr || o == nullptr ||
+      lse == nullptr || d_out == nullptr || dq == nullptr)
+    return LS_ERR_INVALID_ARGUMENT;
+  if (R < 1) return LS_ERR_INVALID_ARGUMENT;
+  if (R >= (int64_t(1) << 31)) return LS_ERR_UNSUPPORTED;
+  if (workspace == nullptr || workspace_bytes < ls_replay_bwd_workspace_bytes(h, R))
+    return LS_ERR_WORKSPACE;
+  if (!aligned16(q) || !aligned16(k_suffix) || !aligned16(v_suffix) || !aligned16(o) ||
+      !aligned16(d_out) || !aligned16(dq) || !aligned16(workspace) || !aligned_n(lse, 4))
+    return LS_ERR_MISALIGNED;
+  uint32_t* status = nullptr;
+  ls_status st = enter(h, stream, &status);
+  if (st != LS_OK) return st;
+
+  BwdArgs a{};
+  a.sh = h->shape;
+  a.sh.P = P_eff;
+  a.sh.R = R;
+  a.tm_kp = &h->tm_k;
+  a.tm_vp = &h->tm_v;
+  const AttnShape& sh = a.sh;
+  st = encode_thd(&a.tm_q, q, R, sh.Hq, sh.D, sh.g, sh.qt);
+  if (st == LS_OK) st = encode_thd(&a.tm_do, d_out, R, sh.Hq, sh.D, sh.g, sh.qt);
+  if (st == LS_OK) st = encode_thd(&a.tm_ks, k_suffix, R, sh.Hkv, sh.D, 1, 128);
+  if (st == LS_OK) st = encode_thd(&a.tm_vs, v_suffix, R, sh.Hkv, sh.D, 1, 128);
+  if (st != LS_OK) return st;
+  float* rowstats = static_cast<float*>(workspace);
+  a.rowstats = rowstats;
+  a.dq = static_cast<uint16_t*>(dq);
+  a.dk_suf = static_cast<uint16_t*>(dk_suffix);
+  a.dv_suf = static_cast<uint16_t*>(dv_suffix);
+  a.dk_acc = h->dk_acc;
+  a.dv_acc = h->dv_acc;
+  a.suffix_to_acc = suffix_to_acc;
+  a.status = status;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  {
+    LaunchTimer t(LS_KERNEL_BWD_PREP, s);
+    e = launch_bwd_prep(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(d_out), lse,
+                        rowstats, sh, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "replay backward prep launch");
+  {
+    LaunchTimer t(LS_KERNEL_BWD_DKDV, s);
+    e = launch_attn_bwd_dkdv(a, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "replay backward dK/dV launch");
+  {
+    LaunchTimer t(LS_KERNEL_BWD_DQ, s);
+    e = launch_attn_bwd_dq(a, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "replay backward dQ launch");
+  return LS_OK;
+}
+
+// out = scale * acc over accumulator rows [row0, row0 + nrows) (fp32 or bf16 out, optional
+// reset), or acc *= scale in place when both outputs are NULL.
+ls_status finalize_impl(ls_prefix_t h, int64_t row0, int64_t nrows, float scale, void* dk_out,
+                        void* dv_out, int out_is_fp32, int reset_acc, void* stream) {
+  if (!std::isfinite(scale)) return LS_ERR_INVALID_ARGUMENT;
+  if ((dk_out == nullptr) != (dv_out == nullptr)) return LS_ERR_INVALID_ARGUMENT;
+  const bool inplace = dk_out == nullptr;
+  if (inplace && reset_acc) return LS_ERR_INVALID_ARGUMENT;
+  if (!inplace && (!aligned16(dk_out) || !aligned16(dv_out))) return LS_ERR_MISALIGNED;
+  uint32_t* status = nullptr;
+  ls_status st = enter(h, stream, &status);
+  if (st != LS_OK) return st;
+  const size_t row = static_cast<size_t>(h->shape.Hkv) * h->shape.D;
+  const size_t n = static_cast<size_t>(nrows) * row;
+  float* dk = h->dk_acc + static_cast<size_t>(row0) * row;
+  float* dv = h->dv_acc + static_cast<size_t>(row0) * row;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  LaunchTimer t(LS_KERNEL_FINALIZE, s);
+  if (inplace) {
+    e = launch_scale_inplace(dk, n, scale, s);
+    if (e == cudaSuccess) e = launch_scale_inplace(dv, n, scale, s);
+  } else {
+    e = launch_finalize(dk, dk_out, n, scale, out_is_fp32 ? 1 : 0, reset_acc ? 1 : 0, s);
+    if (e == cudaSuccess)
+      e = launch_finalize(dv, dv_out, n, scale, out_is_fp32 ? 1 : 0, reset_acc ? 1 : 0, s);
+  }
+  return e == cudaSuccess ? LS_OK : cuda_fail(e, "finalize launch");
+}
+
 }  // namespace
 
 extern "C" {
@@ -311,37 +447,16 @@ ls_status ls_replay_fwd(ls_prefix_t h, int64_t R, const void* q, const void* k_s
                         const void* v_suffix, void* o, float* lse, void* stream) {
   ls_status st = check_handle(h);
   if (st != LS_OK) return st;
-  if (q == nullptr || k_suffix == nullptr || v_suffix == nullptr || o == nullptr ||
-      lse == nullptr)
-    return LS_ERR_INVALID_ARGUMENT;
-  if (R < 1) return LS_ERR_INVALID_ARGUMENT;
-  if (R >= (int64_t(1) << 31)) return LS_ERR_UNSUPPORTED;
-  if (!aligned16(q) || !aligned16(k_suffix) || !aligned16(v_suffix) || !aligned16(o) ||
-      !aligned_n(lse, 4))
-    return LS_ERR_MISALIGNED;
-  uint32_t* status = nullptr;
-  st = enter(h, stream, &status);
-  if (st != LS_OK) return st;
+  return replay_fwd_impl(h, h->shape.P, R, q, k_suffix, v_suffix, o, lse, stream);
+}
 
-  FwdArgs a{};
-  a.sh = h->shape;
-  a.sh.R = R;
-  a.tm_kp = &h->tm_k;
-  a.tm_vp = &h->tm_v;
-  const AttnShape& sh = a.sh;
-  st = encode_thd(&a.tm_q, q, R, sh.Hq, sh.D, sh.g, sh.qt);
-  if (st == LS_OK) st = encode_thd(&a.tm_ks, k_suffix, R, sh.Hkv, sh.D, 1, 128);
-  if (st == LS_OK) st = encode_thd(&a.tm_vs, v_suffix, R, sh.Hkv, sh.D, 1, 128);
+ls_status ls_block_replay_fwd(ls_prefix_t h, int64_t prefix_len, int64_t R, const void* q,
+                              void* o, float* lse, void* stream) {
+  ls_status st = check_handle(h);
   if (st != LS_OK) return st;
-  a.o = static_cast<uint16_t*>(o);
-  a.lse = lse;
-  a.status = status;
-  cudaError_t e;
-  {
-    LaunchTimer t(LS_KERNEL_REPLAY_FWD, static_cast<cudaStream_t>(stream));
-    e = launch_attn_fwd(a, static_cast<cudaStream_t>(stream));
-  }
-  return e == cudaSuccess ? LS_OK : cuda_fail(e, "replay forward launch");
+  if (prefix_len < 1 || R < 1 || prefix_len > h->shape.P - R) return LS_ERR_INVALID_ARGUMENT;
+  return replay_fwd_impl(h, prefix_len, R, q, block_rows(h, h->k_prefix, prefix_len),
+                         block_rows(h, h->v_prefix, prefix_len), o, lse, stream);
 }
 
 size_t ls_replay_bwd_workspace_bytes(ls_prefix_t h, int64_t R) {
@@ -356,60 +471,21 @@ ls_status ls_replay_bwd(ls_prefix_t h, int64_t R, const void* q, const void* k_s
                         void* workspace, size_t workspace_bytes, void* stream) {
   ls_status st = check_handle(h);
   if (st != LS_OK) return st;
-  if (q == nullptr || k_suffix == nullptr || v_suffix == nullptr || o == nullptr ||
-      lse == nullptr || d_out == nullptr || dq == nullptr || dk_suffix == nullptr ||
-      dv_suffix == nullptr)
-    return LS_ERR_INVALID_ARGUMENT;
-  if (R < 1) return LS_ERR_INVALID_ARGUMENT;
-  if (R >= (int64_t(1) << 31)) return LS_ERR_UNSUPPORTED;
-  if (workspace == nullptr || workspace_bytes < ls_replay_bwd_workspace_bytes(h, R))
-    return LS_ERR_WORKSPACE;
-  if (!aligned16(q) || !aligned16(k_suffix) || !aligned16(v_suffix) || !aligned16(o) ||
-      !aligned16(d_out) || !aligned16(dq) || !aligned16(dk_suffix) || !aligned16(dv_suffix) ||
-      !aligned16(workspace) || !aligned_n(lse, 4))
-    return LS_ERR_MISALIGNED;
-  uint32_t* status = nullptr;
-  st = enter(h, stream, &status);
-  if (st != LS_OK) return st;
+  if (dk_suffix == nullptr || dv_suffix == nullptr) return LS_ERR_INVALID_ARGUMENT;
+  if (!aligned16(dk_suffix) || !aligned16(dv_suffix)) return LS_ERR_MISALIGNED;
+  return replay_bwd_impl(h, h->shape.P, R, q, k_suffix, v_suffix, o, lse, d_out, dq, dk_suffix,
+                         dv_suffix, 0, workspace, workspace_bytes, stream);
+}
 
-  BwdArgs a{};
-  a.sh = h->shape;
-  a.sh.R = R;
-  a.tm_kp = &h->tm_k;
-  a.tm_vp = &h->tm_v;
-  const AttnShape& sh = a.sh;
-  st = encode_thd(&a.tm_q, q, R, sh.Hq, sh.D, sh.g, sh.qt);
-  if (st == LS_OK) st = encode_thd(&a.tm_do, d_out, R, sh.Hq, sh.D, sh.g, sh.qt);
-  if (st == LS_OK) st = encode_thd(&a.tm_ks, k_suffix, R, sh.Hkv, sh.D, 1, 128);
-  if (st == LS_OK) st = encode_thd(&a.tm_vs, v_suffix, R, sh.Hkv, sh.D, 1, 128);
+ls_status ls_block_replay_bwd(ls_prefix_t h, int64_t prefix_len, int64_t R, const void* q,
+                              const void* o, const float* lse, const void* d_out, void* dq,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  ls_status st = check_handle(h);
   if (st != LS_OK) return st;
-  float* rowstats = static_cast<float*>(workspace);
-  a.rowstats = rowstats;
-  a.dq = static_cast<uint16_t*>(dq);
-  a.dk_suf = static_cast<uint16_t*>(dk_suffix);
-  a.dv_suf = static_cast<uint16_t*>(dv_suffix);
-  a.dk_acc = h->dk_acc;
-  a.dv_acc = h->dv_acc;
-  a.status = status;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e;
-  {
-    LaunchTimer t(LS_KERNEL_BWD_PREP, s);
-    e = launch_bwd_prep(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(d_out), lse,
-                        rowstats, sh, s);
-  }
-  if (e != cudaSuccess) return cuda_fail(e, "replay backward prep launch");
-  {
-    LaunchTimer t(LS_KERNEL_BWD_DKDV, s);
-    e = launch_attn_bwd_dkdv(a, s);
-  }
-  if (e != cudaSuccess) return cuda_fail(e, "replay backward dK/dV launch");
-  {
-    LaunchTimer t(LS_KERNEL_BWD_DQ, s);
-    e = launch_attn_bwd_dq(a, s);
-  }
-  if (e != cudaSuccess) return cuda_fail(e, "replay backward dQ launch");
-  return LS_OK;
+  if (prefix_len < 1 || R < 1 || prefix_len > h->shape.P - R) return LS_ERR_INVALID_ARGUMENT;
+  return replay_bwd_impl(h, prefix_len, R, q, block_rows(h, h->k_prefix, prefix_len),
+                         block_rows(h, h->v_prefix, prefix_len), o, lse, d_out, dq, nullptr,
+                         nullptr, 1, workspace, workspace_bytes, stream);
 }
 
 size_t ls_grpo_loss_workspace_bytes(int64_t R) {
@@ -489,27 +565,16 @@ ls_status ls_prefix_grad_finalize(ls_prefix_t h, float scale, void* dk_out, void
                                   int out_is_fp32, int reset_acc, void* stream) {
   ls_status st = check_handle(h);
   if (st != LS_OK) return st;
-  if (!std::isfinite(scale)) return LS_ERR_INVALID_ARGUMENT;
-  if ((dk_out == nullptr) != (dv_out == nullptr)) return LS_ERR_INVALID_ARGUMENT;
-  const bool inplace = dk_out == nullptr;
-  if (inplace && reset_acc) return LS_ERR_INVALID_ARGUMENT;
-  if (!inplace && (!aligned16(dk_out) || !aligned16(dv_out))) return LS_ERR_MISALIGNED;
-  uint32_t* status = nullptr;
-  st = enter(h, stream, &status);
+  return finalize_impl(h, 0, h->shape.P, scale, dk_out, dv_out, out_is_fp32, reset_acc, stream);
+}
+
+ls_status ls_prefix_grad_finalize_rows(ls_prefix_t h, int64_t row0, int64_t nrows, float scale,
+                                       void* dk_out, void* dv_out, int out_is_fp32,
+                                       int reset_acc, void* stream) {
+  ls_status st = check_handle(h);
   if (st != LS_OK) return st;
-  const size_t n = static_cast<size_t>(h->shape.P) * h->shape.Hkv * h->shape.D;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e;
-  LaunchTimer t(LS_KERNEL_FINALIZE, s);
-  if (inplace) {
-    e = launch_scale_inplace(h->dk_acc, n, scale, s);
-    if (e == cudaSuccess) e = launch_scale_inplace(h->dv_acc, n, scale, s);
-  } else {
-    e = launch_finalize(h->dk_acc, dk_out, n, scale, out_is_fp32 ? 1 : 0, reset_acc ? 1 : 0, s);
-    if (e == cudaSuccess)
-      e = launch_finalize(h->dv_acc, dv_out, n, scale, out_is_fp32 ? 1 : 0, reset_acc ? 1 : 0, s);
-  }
-  return e == cudaSuccess ? LS_OK : cuda_fail(e, "finalize launch");
+  if (row0 < 0 || nrows < 1 || row0 > h->shape.P - nrows) return LS_ERR_INVALID_ARGUMENT;
+  return finalize_impl(h, row0, nrows, scale, dk_out, dv_out, out_is_fp32, reset_acc, stream);
 }
 
 ls_status ls_debug_wait_timeout(uint64_t limit_ns, void* stream) {

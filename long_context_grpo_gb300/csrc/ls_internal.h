@@ -63,10 +63,11 @@ struct BwdArgs {
   CUtensorMap tm_ks, tm_vs;   // suffix K/V [R][Hkv][D], box {64, 1, 128}
   const float* rowstats;      // [Hkv][n_qt][256]: LSE log2 e of the tile's 128 rows, then Delta
   uint16_t* dq;               // bf16 [R, Hq, D]
-  uint16_t* dk_suf;           // bf16 [R, Hkv, D]
+  uint16_t* dk_suf;           // bf16 [R, Hkv, D] (unused when suffix_to_acc)
   uint16_t* dv_suf;
-  float* dk_acc;              // fp32 [P, Hkv, D]
+  float* dk_acc;              // fp32 [P, Hkv, D] (rows P .. P+R-1 too when suffix_to_acc)
   float* dv_acc;
+  int suffix_to_acc;          // suffix key gradients are added into rows P + key of dk/dv_acc
   uint32_t* status;
 };
 // Row statistics of every 128-row Q tile slot (kv, i, r), r = (t - i qt) g + h - kv g:
