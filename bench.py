@@ -344,6 +344,55 @@ class Group:
                 "attention_activation_bytes_per_block": act(min(block, R)),
                 "attention_activation_bytes_whole": act(R)}
 
+    def packed_replay(self, stream, loss_slot):
+        """The group as one packed (tree) replay: one forward launch for all responses, the
+        G loss calls, one backward launch, one finalize; timed like the serial step after one
+        untimed run.  Returns its time and the extra activation memory it holds."""
+        import torch
+        import long_context_grpo_gb300 as ls
+        w = self.w
+        cu = [0]
+        for Ri in self.R:
+            cu.append(cu[-1] + Ri)
+        q, ks, vs, do = (torch.cat([r[k] for r in self.resp]) for k in ("q", "ks", "vs", "do"))
+        T = cu[-1]
+        o = torch.empty_like(q)
+        lse = torch.empty((T, w.Hq), dtype=torch.float32, device=q.device)
+        dq = torch.empty_like(q)
+        dks = torch.empty_like(ks)
+        dvs = torch.empty_like(vs)
+
+        def step():
+            pre = ls.Prefix(self.kp, self.vp, self.dk_acc, self.dv_acc, Hq=w.Hq)
+            pre.fwd_packed(cu, q, ks, vs, o=o, lse=lse)
+            for i, (r, Ri) in enumerate(zip(self.resp, self.R)):
+                ls.grpo_loss(r["logits"], r["ids"], r["old"], self.A[i], w.eps, w.G, loss_slot,
+                             dlogits=self.dlog[:Ri], clip_mask=self.mask[:Ri],
+                             logp_out=self.logp[:Ri], workspace=self.lws)
+            pre.bwd_packed(cu, q, ks, vs, o, lse, do, dq=dq, dk_suffix=dks, dv_suffix=dvs)
+            pre.finalize(1.0, self.dk_out, self.dv_out)
+            pre.close()
+
+        step()
+        torch.cuda.synchronize()
+        ls.timing_read()
+        ls.timing_enable(True)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ls.timing_enable(False)
+        kt = ls.timing_read()
+        ms = e0.elapsed_time(e1)
+        extra = sum(t.numel() * t.element_size() for t in (q, ks, vs, do, o, lse, dq, dks, dvs))
+        del q, ks, vs, do, o, lse, dq, dks, dvs
+        return {"ms": ms, "tflops": self.flops() / (ms / 1e3) / 1e12,
+                "response_tok_s": sum(self.R) / (ms / 1e3), "launches_attention": 2 + 3,
+                "kernel_ms": {k: round(v[0], 3) for k, v in kt.items() if v[1] > 0},
+                "activation_bytes_held": extra}
+
     def flops(self):
         w = self.w
         return sum(14 * w.D * w.Hq * pairs(w.P, Ri) for Ri in self.R)
@@ -488,6 +537,12 @@ def run_ours(args, w):
     if args.block > 0 and rank == 0:
         blk = grp.block_replay(args.block, stream)
 
+    # ---------------- the group as one packed (tree) replay
+    packed = None
+    if not args.no_packed and rank == 0:
+        packed = grp.packed_replay(stream, losses[0:1])
+        packed["vs_serial_step"] = packed["ms"] and (ms / args.steps) / packed["ms"]
+
     # ---------------- end to end through the C ABI with host buffers
     e2e = None
     if not args.no_e2e:
@@ -554,6 +609,7 @@ def run_ours(args, w):
                 "cpu_baseline": cpu,
                 "scoring": score,
                 "block_replay": blk,
+                "packed_replay": packed,
                 "receipt": {"gradient_semantics": "prompt dK/dV exposed (fp32, group-summed), "
                                                   "not propagated",
                             "residency": "prompt K/V resident in HBM for the group",
@@ -576,6 +632,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-score", action="store_true")
+    ap.add_argument("--no-packed", action="store_true")
     ap.add_argument("--block", type=int, default=4096,
                     help="block length of the blockwise-replay measurement (0: skip it)")
     args = ap.parse_args()

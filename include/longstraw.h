@@ -139,6 +139,31 @@ ls_status ls_replay_bwd(ls_prefix_t h, int64_t R, const void* q, const void* k_s
                         void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Packed replay of several responses in one launch per kernel: the shared-prefix tree
+ * [prompt; y_1; ...; y_G] in which every y_b attends to the prompt and, causally, to itself
+ * only (the prompt as state shared by the group: LongStraw review, section 2; a shared-prefix
+ * tree of trajectories: QwenGyre news article, devotd.net, trajectory-processor paragraph).
+ * Response b owns packed rows cu_seqlens[b] .. cu_seqlens[b+1]-1 of q, k_suffix, v_suffix,
+ * o, lse, d_out, dq, dk_suffix, dv_suffix (THD layouts as for one response, with the packed
+ * row count cu_seqlens[G] in place of R).  cu_seqlens is a HOST array of G+1 int64 values,
+ * cu_seqlens[0] = 0, strictly increasing (every response has at least one token);
+ * 1 <= G <= 64 (LS_ERR_UNSUPPORTED above).  The results are those of G ls_replay_fwd /
+ * ls_replay_bwd calls on the responses one by one; in the backward every prompt 128-key
+ * tile accumulates the contributions of all G responses on chip and is added into the
+ * fp32 accumulators once.  Activation memory grows with G (the serial calls keep it at
+ * one response).
+ */
+ls_status ls_replay_fwd_packed(ls_prefix_t h, int32_t G, const int64_t* cu_seqlens,
+                               const void* q, const void* k_suffix, const void* v_suffix,
+                               void* o, float* lse, void* stream);
+size_t ls_replay_bwd_packed_workspace_bytes(ls_prefix_t h, int32_t G, const int64_t* cu_seqlens);
+ls_status ls_replay_bwd_packed(ls_prefix_t h, int32_t G, const int64_t* cu_seqlens,
+                               const void* q, const void* k_suffix, const void* v_suffix,
+                               const void* o, const float* lse, const void* d_out, void* dq,
+                               void* dk_suffix, void* dv_suffix, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+/*
  * Blockwise suffix replay (review section 3-2 (4), "Blockwise suffix replay": a response is
  * replayed block by block instead of as one graph, which bounds the response's activation
  * peak; attention state has to carry across block boundaries exactly).

@@ -64,6 +64,10 @@ def _load():
         "ls_prefix_grad_finalize_rows": (ctypes.c_int, [vp, i64, i64, ctypes.c_float, vp, vp,
                                                         ctypes.c_int, ctypes.c_int, vp]),
         "ls_block_replay_fwd": (ctypes.c_int, [vp, i64, i64, vp, vp, vp, vp]),
+        "ls_replay_fwd_packed": (ctypes.c_int, [vp, i32, vp, vp, vp, vp, vp, vp, vp]),
+        "ls_replay_bwd_packed_workspace_bytes": (sz, [vp, i32, vp]),
+        "ls_replay_bwd_packed": (ctypes.c_int, [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                                vp, sz, vp]),
         "ls_block_replay_bwd": (ctypes.c_int, [vp, i64, i64, vp, vp, vp, vp, vp, vp, sz, vp]),
         "ls_get_device_status": (ctypes.c_int, [vp, ctypes.POINTER(ctypes.c_uint32)]),
         "ls_timing_enable": (ctypes.c_int, [ctypes.c_int]),
@@ -188,6 +192,56 @@ class Prefix:
             _ptr(dv_suffix, "dv_suffix", torch.bfloat16, (R, self.Hkv, self.D)),
             _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream()),
             "ls_replay_bwd")
+        return dq, dk_suffix, dv_suffix
+
+    @staticmethod
+    def _cu(cu_seqlens):
+        cu = [int(x) for x in cu_seqlens]
+        return len(cu) - 1, (ctypes.c_int64 * len(cu))(*cu), cu[-1]
+
+    def fwd_packed(self, cu_seqlens, q, k_suffix, v_suffix, o=None, lse=None):
+        """One launch for G responses packed along the token axis: response b owns rows
+        cu_seqlens[b] .. cu_seqlens[b+1]-1 and sees the prompt and, causally, itself."""
+        G, cu, T = self._cu(cu_seqlens)
+        if o is None:
+            o = torch.empty_like(q)
+        if lse is None:
+            lse = torch.empty((T, self.Hq), dtype=torch.float32, device=q.device)
+        _check(_lib().ls_replay_fwd_packed(
+            self._h, G, ctypes.cast(cu, ctypes.c_void_p),
+            _ptr(q, "q", torch.bfloat16, (T, self.Hq, self.D)),
+            _ptr(k_suffix, "k_suffix", torch.bfloat16, (T, self.Hkv, self.D)),
+            _ptr(v_suffix, "v_suffix", torch.bfloat16, (T, self.Hkv, self.D)),
+            _ptr(o, "o", torch.bfloat16, (T, self.Hq, self.D)),
+            _ptr(lse, "lse", torch.float32, (T, self.Hq)), _stream()), "ls_replay_fwd_packed")
+        return o, lse
+
+    def bwd_packed_workspace_bytes(self, cu_seqlens) -> int:
+        G, cu, _ = self._cu(cu_seqlens)
+        return int(_lib().ls_replay_bwd_packed_workspace_bytes(self._h, G, ctypes.cast(cu, ctypes.c_void_p)))
+
+    def bwd_packed(self, cu_seqlens, q, k_suffix, v_suffix, o, lse, d_out, dq=None,
+                   dk_suffix=None, dv_suffix=None, workspace=None):
+        G, cu, T = self._cu(cu_seqlens)
+        dq = torch.empty_like(q) if dq is None else dq
+        dk_suffix = torch.empty_like(k_suffix) if dk_suffix is None else dk_suffix
+        dv_suffix = torch.empty_like(v_suffix) if dv_suffix is None else dv_suffix
+        if workspace is None:
+            workspace = torch.empty(max(self.bwd_packed_workspace_bytes(cu_seqlens), 16),
+                                    dtype=torch.uint8, device=q.device)
+        _check(_lib().ls_replay_bwd_packed(
+            self._h, G, ctypes.cast(cu, ctypes.c_void_p),
+            _ptr(q, "q", torch.bfloat16, (T, self.Hq, self.D)),
+            _ptr(k_suffix, "k_suffix", torch.bfloat16, (T, self.Hkv, self.D)),
+            _ptr(v_suffix, "v_suffix", torch.bfloat16, (T, self.Hkv, self.D)),
+            _ptr(o, "o", torch.bfloat16, (T, self.Hq, self.D)),
+            _ptr(lse, "lse", torch.float32, (T, self.Hq)),
+            _ptr(d_out, "d_out", torch.bfloat16, (T, self.Hq, self.D)),
+            _ptr(dq, "dq", torch.bfloat16, (T, self.Hq, self.D)),
+            _ptr(dk_suffix, "dk_suffix", torch.bfloat16, (T, self.Hkv, self.D)),
+            _ptr(dv_suffix, "dv_suffix", torch.bfloat16, (T, self.Hkv, self.D)),
+            _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream()),
+            "ls_replay_bwd_packed")
         return dq, dk_suffix, dv_suffix
 
     def block_fwd(self, prefix_len: int, q, o=None, lse=None):

@@ -79,25 +79,60 @@ struct DkdvCfg {
 struct KvUnit {
   int kv;
   bool prompt;
-  int key0;   // first key of the tile (prompt or suffix index)
-  int i0;     // first 128-row Q tile
+  int key0;   // first key of the tile (prompt index, or response-local suffix index)
+  int base;   // suffix tiles: packed row of the response's first token
+  int R;      // suffix tiles: response length
+  int b;      // suffix tiles: response
+  int f0;     // first flat 128-row Q tile that sees the tile
   int n;      // number of Q tiles
 };
 
-__device__ __forceinline__ KvUnit make_kv_unit(int u, const AttnShape& sh, int n_qt) {
+// Flat unit u -> (kv head, 128-key tile).  A prompt tile is seen by every Q tile of every
+// packed response; a suffix tile of response b by that response's tiles from the first
+// one holding a query at or after its first key.
+template <bool kPacked>
+__device__ __forceinline__ KvUnit make_kv_unit(int u, const AttnShape& sh, const Varlen& vl) {
   const int n_pt = static_cast<int>((sh.P + 127) / 128);
-  const int n_st = static_cast<int>((sh.R + 127) / 128);
   KvUnit w;
+  if constexpr (!kPacked) {
+    // one response: base 0, length sh.R
+    const int n_st = static_cast<int>((sh.R + 127) / 128);
+    const int n_qt = static_cast<int>((sh.R + sh.qt - 1) / sh.qt);
+    w.kv = u / (n_pt + n_st);
+    const int j = u - w.kv * (n_pt + n_st);
+    w.prompt = j < n_pt;
+    w.key0 = w.prompt ? 128 * j : 128 * (j - n_pt);
+    w.base = 0;
+    w.R = static_cast<int>(sh.R);
+    w.b = 0;
+    w.f0 = w.prompt ? 0 : w.key0 / sh.qt;
+    w.n = n_qt - w.f0;
+    return w;
+  }
+  const int n_st = vl.kt0[vl.G];
   w.kv = u / (n_pt + n_st);
   const int j = u - w.kv * (n_pt + n_st);
   w.prompt = j < n_pt;
-  w.key0 = w.prompt ? 128 * j : 128 * (j - n_pt);
-  w.i0 = w.prompt ? 0 : w.key0 / sh.qt;
-  w.n = n_qt - w.i0;
+  if (w.prompt) {
+    w.key0 = 128 * j;
+    w.base = 0;
+    w.R = 0;
+    w.b = 0;
+    w.f0 = 0;
+    w.n = vl.qt0[vl.G];
+  } else {
+    const int x = j - n_pt;
+    w.b = varlen_find(vl.kt0, vl.G, x);
+    w.key0 = 128 * (x - vl.kt0[w.b]);
+    w.base = vl.row0[w.b];
+    w.R = vl.row0[w.b + 1] - w.base;
+    w.f0 = vl.qt0[w.b] + w.key0 / sh.qt;
+    w.n = vl.qt0[w.b + 1] - w.f0;
+  }
   return w;
 }
 
-template <int D>
+template <int D, bool kPacked>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_kp,
                          const __grid_constant__ CUtensorMap tm_vp,
@@ -108,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const float* __restrict__ rowstats, float* __restrict__ dk_acc,
                          float* __restrict__ dv_acc, uint16_t* __restrict__ dk_suf,
                          uint16_t* __restrict__ dv_suf, const int suffix_to_acc,
-                         uint32_t* status) {
+                         const __grid_constant__ Varlen vl, uint32_t* status) {
   using C = DkdvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -118,8 +153,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_qt = static_cast<int>((sh.R + sh.qt - 1) / sh.qt);
-  const int n_units = sh.Hkv * static_cast<int>((sh.P + 127) / 128 + (sh.R + 127) / 128);
+  const int n_qt = kPacked ? vl.qt0[vl.G] : static_cast<int>((sh.R + sh.qt - 1) / sh.qt);
+  const int n_units = sh.Hkv * (static_cast<int>((sh.P + 127) / 128) +
+                                (kPacked ? vl.kt0[vl.G] : static_cast<int>((sh.R + 127) / 128)));
   const int rows_used = sh.g * sh.qt;   // rows of a 128-row tile that TMA fills
 
   // Padding rows of every Q/dO buffer are never written by TMA: zero them once so that
@@ -183,19 +219,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t qit = 0, uc = 0;
       bool ok = true, kv_pending = false;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
-        const KvUnit w = make_kv_unit(u, sh, n_qt);
+        const KvUnit w = make_kv_unit<kPacked>(u, sh, vl);
         if (uc > 0) ok = mbar_wait(&bars[C::kBarKVEmpty], (uc - 1) & 1u, status, vabort);
         if (!ok) break;
         mbar_arrive_expect_tx(&bars[C::kBarKVFull], 2 * C::kTile);
         for (int b = 0; b < C::kBoxes; ++b) {
           tma_load_3d(smem + C::kOffK + b * 16384, w.prompt ? &tm_kp : &tm_ks,
-                      &bars[C::kBarKVFull], 64 * b, w.kv, w.key0);
+                      &bars[C::kBarKVFull], 64 * b, w.kv, w.base + w.key0);
           tma_load_3d(smem + C::kOffV + b * 16384, w.prompt ? &tm_vp : &tm_vs,
-                      &bars[C::kBarKVFull], 64 * b, w.kv, w.key0);
+                      &bars[C::kBarKVFull], 64 * b, w.kv, w.base + w.key0);
         }
         kv_pending = true;
+        int rb = w.prompt ? 0 : w.b;   // response of the current Q tile
         for (int li = 0; li < w.n && ok; ++li, ++qit) {
-          const int i = w.i0 + li;
+          const int f = w.f0 + li;
+          int qrow = f * sh.qt;         // packed row of the tile
+          if constexpr (kPacked) {
+            while (f >= vl.qt0[rb + 1]) ++rb;
+            qrow = vl.row0[rb] + (f - vl.qt0[rb]) * sh.qt;
+          }
           const uint32_t sq = qit % C::kNQ, so = qit % C::kNO;
           if (qit >= static_cast<uint32_t>(C::kNQ))
             ok = mbar_wait(&bars[C::kBarQEmpty + sq], ((qit / C::kNQ) - 1) & 1u, status, vabort);
@@ -203,14 +245,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&bars[C::kBarQFull + sq], tile_tx);
           for (int b = 0; b < C::kBoxes; ++b)
             tma_load_3d(smem + C::kOffQ + sq * C::kTile + b * 16384, &tm_q,
-                        &bars[C::kBarQFull + sq], 64 * b, w.kv * sh.g, i * sh.qt);
+                        &bars[C::kBarQFull + sq], 64 * b, w.kv * sh.g, qrow);
           if (qit >= static_cast<uint32_t>(C::kNO))
             ok = mbar_wait(&bars[C::kBarOEmpty + so], ((qit / C::kNO) - 1) & 1u, status, vabort);
           if (!ok) break;
           mbar_arrive_expect_tx(&bars[C::kBarOFull + so], tile_tx);
           for (int b = 0; b < C::kBoxes; ++b)
             tma_load_3d(smem + C::kOffO + so * C::kTile + b * 16384, &tm_do,
-                        &bars[C::kBarOFull + so], 64 * b, w.kv * sh.g, i * sh.qt);
+                        &bars[C::kBarOFull + so], 64 * b, w.kv * sh.g, qrow);
         }
       }
       if (!ok) {
@@ -281,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&bars[C::kBarOEmpty + it % C::kNO]);
       };
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
-        const KvUnit w = make_kv_unit(u, sh, n_qt);
+        const KvUnit w = make_kv_unit<kPacked>(u, sh, vl);
         ok = mbar_wait(&bars[C::kBarKVFull], uc & 1u, status, vabort);
         if (!ok) break;
         tc_fence_after();
@@ -323,11 +365,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t qit = 0u, uc = 0u, n_tiles = 0u;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
-      const KvUnit w = make_kv_unit(u, sh, n_qt);
+      const KvUnit w = make_kv_unit<kPacked>(u, sh, vl);
       const int key = w.key0 + row;
       for (int li = 0; li < w.n; ++li, ++n_tiles) {
         // row statistics of this Q tile: every thread reads the same 1 KB (L1 broadcast)
-        const float* rs = rowstats + (static_cast<int64_t>(w.kv) * n_qt + w.i0 + li) * 256;
+        const float* rs = rowstats + (static_cast<int64_t>(w.kv) * n_qt + w.f0 + li) * 256;
         const float4* lse4 = reinterpret_cast<const float4*>(rs) + wg * 16;   // rows 64 wg ..
         const float4* dlt4 = reinterpret_cast<const float4*>(rs + 128) + wg * 16;
         ok = mbar_wait(&bars[C::kBarSFull], n_tiles & 1u, status, vabort);
@@ -362,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // causal suffix: rows r < lo of the tile see only suffix keys < this key
         if (!w.prompt) {
-          const int v = sh.g * (key - (w.i0 + li) * sh.qt);
+          const int v = sh.g * (key - (w.f0 + li - (kPacked ? vl.qt0[w.b] : 0)) * sh.qt);
           const int lo = v < 0 ? 0 : (v > 128 ? 128 : v);
           if (lo > wg * 64) {
 #pragma unroll
@@ -409,10 +451,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const bool valid = w.prompt ? (key < sh.P) : (key < sh.R);
+      const bool valid = w.prompt ? (key < sh.P) : (key < w.R);
       const uint32_t col = wg == 0 ? C::kColDV : C::kColDK;
       const float mul = wg == 0 ? 1.0f : sh.scale;
-      const int64_t off = (static_cast<int64_t>(key) * sh.Hkv + w.kv) * D;
+      const int64_t off = ((static_cast<int64_t>(w.base) + key) * sh.Hkv + w.kv) * D;
       // fp32 accumulation: prompt keys, and suffix keys in block replay (rows P + key)
       const bool to_acc = w.prompt || suffix_to_acc != 0;
       const int64_t off_acc = w.prompt ? off : ((sh.P + key) * sh.Hkv + w.kv) * D;
@@ -494,17 +536,22 @@ struct DqCfg {
 
 struct QUnit {
   int kv;
-  int t0;      // first query of the tile
-  int i;       // tile index
+  int f;       // flat 128-row Q tile over the packed responses
+  int base;    // packed row of the response's first token
+  int R;       // response length
+  int t0;      // first query of the tile (response-local)
   int n_pt;    // prompt 128-key steps
   int n;       // total steps
 };
 
+// One response (base 0, length sh.R): flat unit u -> (kv head, 128-row Q tile).
 __device__ __forceinline__ QUnit make_q_unit(int u, const AttnShape& sh, int n_qt) {
   QUnit w;
   w.kv = u / n_qt;
-  w.i = u - w.kv * n_qt;
-  w.t0 = w.i * sh.qt;
+  w.f = u - w.kv * n_qt;
+  w.base = 0;
+  w.R = static_cast<int>(sh.R);
+  w.t0 = w.f * sh.qt;
   int t_end = w.t0 + sh.qt;
   if (t_end > sh.R) t_end = static_cast<int>(sh.R);
   w.n_pt = static_cast<int>((sh.P + 127) / 128);
@@ -512,7 +559,30 @@ __device__ __forceinline__ QUnit make_q_unit(int u, const AttnShape& sh, int n_q
   return w;
 }
 
-template <int D>
+// Packed responses: flat unit u -> (kv head, flat Q tile f of response b).
+__device__ __forceinline__ QUnit make_q_unit_packed(int u, const AttnShape& sh, const Varlen& vl) {
+  QUnit w;
+  const int n_qt = vl.qt0[vl.G];
+  w.kv = u / n_qt;
+  w.f = u - w.kv * n_qt;
+  const int b = varlen_find(vl.qt0, vl.G, w.f);
+  w.base = vl.row0[b];
+  w.R = vl.row0[b + 1] - w.base;
+  w.t0 = (w.f - vl.qt0[b]) * sh.qt;
+  int t_end = w.t0 + sh.qt;
+  if (t_end > w.R) t_end = w.R;
+  w.n_pt = static_cast<int>((sh.P + 127) / 128);
+  w.n = w.n_pt + (t_end + 127) / 128;
+  return w;
+}
+
+template <bool kPacked>
+__device__ __forceinline__ QUnit pick_q_unit(int u, const AttnShape& sh, int n_qt, const Varlen& vl) {
+  if constexpr (kPacked) return make_q_unit_packed(u, sh, vl);
+  else return make_q_unit(u, sh, n_qt);
+}
+
+template <int D, bool kPacked>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_kp,
                        const __grid_constant__ CUtensorMap tm_vp,
@@ -521,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_do, const AttnShape sh,
                        const float* __restrict__ rowstats, uint16_t* __restrict__ dq,
-                       uint32_t* status) {
+                       const __grid_constant__ Varlen vl, uint32_t* status) {
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -531,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_qt = static_cast<int>((sh.R + sh.qt - 1) / sh.qt);
+  const int n_qt = kPacked ? vl.qt0[vl.G] : static_cast<int>((sh.R + sh.qt - 1) / sh.qt);
   const int n_units = sh.Hkv * n_qt;
 
   if (threadIdx.x == 0) {
@@ -579,20 +649,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t kit = 0, uc = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
-        const QUnit w = make_q_unit(u, sh, n_qt);
+        const QUnit w = pick_q_unit<kPacked>(u, sh, n_qt, vl);
         if (uc > 0) ok = mbar_wait(&bars[C::kBarQEmpty], (uc - 1) & 1u, status, vabort);
         if (!ok) break;
         mbar_arrive_expect_tx(&bars[C::kBarQFull],
                               static_cast<uint32_t>(2 * C::kBoxes * 128 * sh.g * sh.qt));
         for (int b = 0; b < C::kBoxes; ++b) {
           tma_load_3d(smem + C::kOffQ + b * 16384, &tm_q, &bars[C::kBarQFull], 64 * b,
-                      w.kv * sh.g, w.t0);
+                      w.kv * sh.g, (kPacked ? w.base : 0) + w.t0);
           tma_load_3d(smem + C::kOffDO + b * 16384, &tm_do, &bars[C::kBarQFull], 64 * b,
-                      w.kv * sh.g, w.t0);
+                      w.kv * sh.g, (kPacked ? w.base : 0) + w.t0);
         }
         for (int j = 0; j < w.n && ok; ++j, ++kit) {
           const bool pre = j < w.n_pt;
-          const int key0 = pre ? 128 * j : 128 * (j - w.n_pt);
+          const int key0 = pre ? 128 * j : (kPacked ? w.base : 0) + 128 * (j - w.n_pt);
           const uint32_t sk = kit % C::kNK, sv = kit % C::kNV;
           if (kit >= static_cast<uint32_t>(C::kNK))
             ok = mbar_wait(&bars[C::kBarKEmpty + sk], ((kit / C::kNK) - 1) & 1u, status, vabort);
@@ -673,7 +743,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&bars[C::kBarKEmpty + sk]);
       };
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
-        const QUnit w = make_q_unit(u, sh, n_qt);
+        const QUnit w = pick_q_unit<kPacked>(u, sh, n_qt, vl);
         ok = mbar_wait(&bars[C::kBarQTmem], uc & 1u, status, vabort);
         if (!ok) break;
         tc_fence_after();
@@ -714,13 +784,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t uc = 0u, n_steps = 0u;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
-      const QUnit w = make_q_unit(u, sh, n_qt);
+      const QUnit w = pick_q_unit<kPacked>(u, sh, n_qt, vl);
       const int t = w.t0 + row / sh.g;
       const int hg = row % sh.g;
-      const bool valid = (row < sh.g * sh.qt) && (t < sh.R);
+      const bool valid = (row < sh.g * sh.qt) && (kPacked ? t < w.R : t < sh.R);
       float lse2 = INFINITY, dlt = 0.0f;
       if (valid) {
-        const float* rs = rowstats + (static_cast<int64_t>(w.kv) * n_qt + w.i) * 256;
+        const float* rs = rowstats + (static_cast<int64_t>(w.kv) * n_qt + w.f) * 256;
         lse2 = rs[row];
         dlt = rs[128 + row];
       }
@@ -813,7 +883,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const int h = w.kv * sh.g + hg;
-      uint16_t* drow = dq + (static_cast<int64_t>(t) * sh.Hq + h) * D;
+      uint16_t* drow = dq + ((kPacked ? static_cast<int64_t>(w.base) + t : static_cast<int64_t>(t)) * sh.Hq + h) * D;
 #pragma unroll
       for (int cc = 0; cc < D / 64; ++cc) {
         const int col = wg * (D / 2) + cc * 32;
@@ -847,53 +917,55 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool kPacked>
 cudaError_t launch_dkdv_d(const BwdArgs& a, cudaStream_t s) {
   using C = DkdvCfg<D>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D, kPacked>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   const int64_t n_units =
-      static_cast<int64_t>(a.sh.Hkv) * ((a.sh.P + 127) / 128 + (a.sh.R + 127) / 128);
+      static_cast<int64_t>(a.sh.Hkv) * ((a.sh.P + 127) / 128 + a.vl.kt0[a.vl.G]);
   int grid = num_sms();
   if (n_units < grid) grid = static_cast<int>(n_units);
-  attn_bwd_dkdv_kernel<D><<<grid, kThreads, C::kSmem, s>>>(
+  attn_bwd_dkdv_kernel<D, kPacked><<<grid, kThreads, C::kSmem, s>>>(
       *a.tm_kp, *a.tm_vp, a.tm_ks, a.tm_vs, a.tm_q, a.tm_do, a.sh, a.rowstats, a.dk_acc,
-      a.dv_acc, a.dk_suf, a.dv_suf, a.suffix_to_acc, a.status);
+      a.dv_acc, a.dk_suf, a.dv_suf, a.suffix_to_acc, a.vl, a.status);
   return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool kPacked>
 cudaError_t launch_dq_d(const BwdArgs& a, cudaStream_t s) {
   using C = DqCfg<D>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_dq_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_dq_kernel<D, kPacked>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int64_t n_units = static_cast<int64_t>(a.sh.Hkv) * ((a.sh.R + a.sh.qt - 1) / a.sh.qt);
+  const int64_t n_units = static_cast<int64_t>(a.sh.Hkv) * a.vl.qt0[a.vl.G];
   int grid = num_sms();
   if (n_units < grid) grid = static_cast<int>(n_units);
-  attn_bwd_dq_kernel<D><<<grid, kThreads, C::kSmem, s>>>(*a.tm_kp, *a.tm_vp, a.tm_ks, a.tm_vs,
+  attn_bwd_dq_kernel<D, kPacked><<<grid, kThreads, C::kSmem, s>>>(*a.tm_kp, *a.tm_vp, a.tm_ks, a.tm_vs,
                                                         a.tm_q, a.tm_do, a.sh, a.rowstats, a.dq,
-                                                        a.status);
+                                                        a.vl, a.status);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_attn_bwd_dkdv(const BwdArgs& a, cudaStream_t s) {
-  return a.sh.D == 128 ? launch_dkdv_d<128>(a, s) : launch_dkdv_d<64>(a, s);
+  if (a.vl.G > 1) return a.sh.D == 128 ? launch_dkdv_d<128, true>(a, s) : launch_dkdv_d<64, true>(a, s);
+  return a.sh.D == 128 ? launch_dkdv_d<128, false>(a, s) : launch_dkdv_d<64, false>(a, s);
 }
 
 cudaError_t launch_attn_bwd_dq(const BwdArgs& a, cudaStream_t s) {
-  return a.sh.D == 128 ? launch_dq_d<128>(a, s) : launch_dq_d<64>(a, s);
+  if (a.vl.G > 1) return a.sh.D == 128 ? launch_dq_d<128, true>(a, s) : launch_dq_d<64, true>(a, s);
+  return a.sh.D == 128 ? launch_dq_d<128, false>(a, s) : launch_dq_d<64, false>(a, s);
 }
 
 }  // namespace ls

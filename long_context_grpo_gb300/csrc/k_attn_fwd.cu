@@ -61,17 +61,23 @@ struct FwdCfg {
 
 struct Unit {
   int kv;
-  int t0;        // first query of Q tile 0
+  int base;      // packed row of the response's first token
+  int R;         // response length
+  int t0;        // first query of Q tile 0 (response-local)
   bool has1;     // Q tile 1 exists
   int n_pt;      // prompt key tiles
   int n_kt;      // total key tiles
 };
 
+// Flat unit u -> (kv head, pair of Q tiles) of one response (base 0, length sh.R); kv-major
+// so concurrently running CTAs stream the same prompt K/V.
 __device__ __forceinline__ Unit make_unit(int u, const AttnShape& sh, int n_pairs) {
   Unit w;
   w.kv = u / n_pairs;
   const int pair = u - w.kv * n_pairs;
   const int n_qt = static_cast<int>((sh.R + sh.qt - 1) / sh.qt);
+  w.base = 0;
+  w.R = static_cast<int>(sh.R);
   w.t0 = pair * 2 * sh.qt;
   w.has1 = (2 * pair + 1) < n_qt;
   int t_end = w.t0 + (w.has1 ? 2 : 1) * sh.qt;
@@ -81,15 +87,41 @@ __device__ __forceinline__ Unit make_unit(int u, const AttnShape& sh, int n_pair
   return w;
 }
 
-template <int D>
+// Packed responses: flat unit u -> (kv head, response, pair of that response's Q tiles).
+__device__ __forceinline__ Unit make_unit_packed(int u, const AttnShape& sh, const Varlen& vl) {
+  Unit w;
+  const int n_pairs = vl.pair0[vl.G];
+  w.kv = u / n_pairs;
+  const int x = u - w.kv * n_pairs;
+  const int b = varlen_find(vl.pair0, vl.G, x);
+  const int pair = x - vl.pair0[b];
+  w.base = vl.row0[b];
+  w.R = vl.row0[b + 1] - w.base;
+  const int n_qt = (w.R + sh.qt - 1) / sh.qt;
+  w.t0 = pair * 2 * sh.qt;
+  w.has1 = (2 * pair + 1) < n_qt;
+  int t_end = w.t0 + (w.has1 ? 2 : 1) * sh.qt;
+  if (t_end > w.R) t_end = w.R;
+  w.n_pt = static_cast<int>((sh.P + 127) / 128);
+  w.n_kt = w.n_pt + (t_end + 127) / 128;
+  return w;
+}
+
+template <bool kPacked>
+__device__ __forceinline__ Unit pick_unit(int u, const AttnShape& sh, int n_pairs, const Varlen& vl) {
+  if constexpr (kPacked) return make_unit_packed(u, sh, vl);
+  else return make_unit(u, sh, n_pairs);
+}
+
+template <int D, bool kPacked>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_kp,
                     const __grid_constant__ CUtensorMap tm_vp,
                     const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_ks,
                     const __grid_constant__ CUtensorMap tm_vs, const AttnShape sh,
-                    uint16_t* __restrict__ o_out, float* __restrict__ lse_out,
-                    uint32_t* status) {
+                    const __grid_constant__ Varlen vl, uint16_t* __restrict__ o_out,
+                    float* __restrict__ lse_out, uint32_t* status) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -100,7 +132,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n_pairs = static_cast<int>(((sh.R + sh.qt - 1) / sh.qt + 1) / 2);
+  const int n_pairs = kPacked ? vl.pair0[vl.G]
+                              : static_cast<int>(((sh.R + sh.qt - 1) / sh.qt + 1) / 2);
   const int n_units = sh.Hkv * n_pairs;
 
   if (threadIdx.x == 0) {
@@ -146,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t kit = 0, vit = 0, uc = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
-        const Unit w = make_unit(u, sh, n_pairs);
+        const Unit w = pick_unit<kPacked>(u, sh, n_pairs, vl);
         if (uc > 0) ok = mbar_wait(&bars[C::kBarQEmpty], (uc - 1) & 1u, status);
         if (!ok) break;
         const int nq = w.has1 ? 2 : 1;
@@ -155,10 +188,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < nq; ++q)
           for (int b = 0; b < C::kBoxes; ++b)
             tma_load_3d(smem + C::kOffQ + q * C::kTile + b * 16384, &tm_q, &bars[C::kBarQFull],
-                        64 * b, w.kv * sh.g, w.t0 + q * sh.qt);
+                        64 * b, w.kv * sh.g, (kPacked ? w.base : 0) + w.t0 + q * sh.qt);
         for (int j = 0; j < w.n_kt && ok; ++j) {
           const bool pre = j < w.n_pt;
-          const int key0 = pre ? 128 * j : 128 * (j - w.n_pt);
+          const int key0 = pre ? 128 * j : (kPacked ? w.base : 0) + 128 * (j - w.n_pt);
           {
             const uint32_t s = kit % C::kNK;
             if (kit >= static_cast<uint32_t>(C::kNK))
@@ -231,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
 
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
-        const Unit w = make_unit(u, sh, n_pairs);
+        const Unit w = pick_unit<kPacked>(u, sh, n_pairs, vl);
         const int nq = w.has1 ? 2 : 1;
         ok = mbar_wait(&bars[C::kBarQFull], uc & 1u, status, vabort);
         if (!ok) break;
@@ -304,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t sph = 0u, uq = 0u;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-      const Unit w = make_unit(u, sh, n_pairs);
+      const Unit w = pick_unit<kPacked>(u, sh, n_pairs, vl);
       if (q == 1 && !w.has1) continue;
       const int t = w.t0 + q * sh.qt + row / sh.g;
       float m_run = -INFINITY, l = 0.0f;
@@ -387,10 +420,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const bool valid = (row < sh.g * sh.qt) && (t < sh.R);
+      const bool valid = (row < sh.g * sh.qt) && (kPacked ? t < w.R : t < sh.R);
       const int h = w.kv * sh.g + row % sh.g;
       const float inv_l = (l > 0.0f) ? 1.0f / l : 0.0f;
-      uint16_t* orow = o_out + (static_cast<int64_t>(t) * sh.Hq + h) * D;
+      const int64_t prow = kPacked ? static_cast<int64_t>(w.base) + t : static_cast<int64_t>(t);
+      uint16_t* orow = o_out + (prow * sh.Hq + h) * D;
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t ov[32];
@@ -409,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (valid) lse_out[static_cast<int64_t>(t) * sh.Hq + h] = (m_run + __log2f(l)) * kLn2;
+      if (valid) lse_out[prow * sh.Hq + h] = (m_run + __log2f(l)) * kLn2;
       tc_fence_before();
       mbar_arrive(&bars[C::kBarOFree + q]);
       ++uq;
@@ -425,29 +459,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool kPacked>
 cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t s) {
   using C = FwdCfg<D>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, kPacked>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int64_t n_qt = (a.sh.R + a.sh.qt - 1) / a.sh.qt;
-  const int64_t n_units = static_cast<int64_t>(a.sh.Hkv) * ((n_qt + 1) / 2);
+  const int64_t n_units = static_cast<int64_t>(a.sh.Hkv) * a.vl.pair0[a.vl.G];
   int grid = num_sms();
   if (n_units < grid) grid = static_cast<int>(n_units);
-  attn_fwd_kernel<D><<<grid, kThreads, C::kSmem, s>>>(*a.tm_kp, *a.tm_vp, a.tm_q, a.tm_ks,
-                                                      a.tm_vs, a.sh, a.o, a.lse, a.status);
+  attn_fwd_kernel<D, kPacked><<<grid, kThreads, C::kSmem, s>>>(
+      *a.tm_kp, *a.tm_vp, a.tm_q, a.tm_ks, a.tm_vs, a.sh, a.vl, a.o, a.lse, a.status);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t s) {
-  return a.sh.D == 128 ? launch_fwd_d<128>(a, s) : launch_fwd_d<64>(a, s);
+  if (a.vl.G > 1) return a.sh.D == 128 ? launch_fwd_d<128, true>(a, s) : launch_fwd_d<64, true>(a, s);
+  return a.sh.D == 128 ? launch_fwd_d<128, false>(a, s) : launch_fwd_d<64, false>(a, s);
 }
 
 }  // namespace ls

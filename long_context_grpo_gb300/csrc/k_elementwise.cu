@@ -61,27 +61,30 @@ __global__ void __launch_bounds__(kThreads) scale_kernel(float4* acc, size_t n4,
 // 128 LSE values, then the 128 Delta values.
 __global__ void __launch_bounds__(kThreads) bwd_prep_kernel(const uint4* o, const uint4* d_out,
                                                            const float* lse, float* rowstats,
-                                                           AttnShape sh, int64_t n_qt) {
+                                                           AttnShape sh,
+                                                           const __grid_constant__ Varlen vl) {
   const int lane = threadIdx.x & 31;
   const int64_t warps_total = static_cast<int64_t>(gridDim.x) * (kThreads / 32);
   const int per_row = sh.D / 8;   // 8 or 16 lanes, 8 bf16 each
+  const int64_t n_qt = vl.qt0[vl.G];
   const int64_t slots = static_cast<int64_t>(sh.Hkv) * n_qt * 128;
   for (int64_t sidx = blockIdx.x * static_cast<int64_t>(kThreads / 32) + (threadIdx.x >> 5);
        sidx < slots; sidx += warps_total) {
-    const int64_t tile = sidx >> 7;                // kv * n_qt + i
+    const int64_t tile = sidx >> 7;                // kv * n_qt + f
     const int r = static_cast<int>(sidx & 127);
     const int64_t kv = tile / n_qt;
-    const int64_t i = tile - kv * n_qt;
-    const int64_t t = i * sh.qt + r / sh.g;
+    const int f = static_cast<int>(tile - kv * n_qt);
+    const int b = varlen_find(vl.qt0, vl.G, f);
+    const int64_t t = static_cast<int64_t>(f - vl.qt0[b]) * sh.qt + r / sh.g;
     const int64_t h = kv * sh.g + r % sh.g;
-    const bool valid = (r < sh.g * sh.qt) && (t < sh.R);
+    const bool valid = (r < sh.g * sh.qt) && (t < vl.row0[b + 1] - vl.row0[b]);
+    const int64_t row = (vl.row0[b] + t) * sh.Hq + h;
     float acc = 0.f;
     if (valid && lane < per_row) {
-      const int64_t row = t * sh.Hq + h;
       const uint4 a = __ldcs(o + row * per_row + lane);
-      const uint4 b = __ldcs(d_out + row * per_row + lane);
+      const uint4 bb = __ldcs(d_out + row * per_row + lane);
       const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
-      const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+      const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         acc = fmaf(__uint_as_float(aw[k] << 16), __uint_as_float(bw[k] << 16), acc);
@@ -92,7 +95,7 @@ __global__ void __launch_bounds__(kThreads) bwd_prep_kernel(const uint4* o, cons
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (lane == 0) {
       float* dst = rowstats + tile * 256;
-      dst[r] = valid ? lse[t * sh.Hq + h] * 1.4426950408889634f : INFINITY;
+      dst[r] = valid ? lse[row] * 1.4426950408889634f : INFINITY;
       dst[128 + r] = valid ? acc : 0.f;
     }
   }
@@ -152,12 +155,12 @@ cudaError_t launch_wait_timeout(uint64_t limit_ns, uint32_t* status, cudaStream_
 }
 
 cudaError_t launch_bwd_prep(const uint16_t* o, const uint16_t* d_out, const float* lse,
-                            float* rowstats, const AttnShape& sh, cudaStream_t s) {
-  const int64_t n_qt = (sh.R + sh.qt - 1) / sh.qt;
-  const size_t slots = static_cast<size_t>(sh.Hkv) * n_qt * 128;
+                            float* rowstats, const AttnShape& sh, const Varlen& vl,
+                            cudaStream_t s) {
+  const size_t slots = static_cast<size_t>(sh.Hkv) * vl.qt0[vl.G] * 128;
   bwd_prep_kernel<<<grid_for(slots * 32), kThreads, 0, s>>>(
       reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(d_out), lse, rowstats, sh,
-      n_qt);
+      vl);
   return cudaGetLastError();
 }
 

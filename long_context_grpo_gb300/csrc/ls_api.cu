@@ -218,26 +218,47 @@ const void* block_rows(ls_prefix_t h, const void* base, int64_t row0) {
   return static_cast<const uint16_t*>(base) + row0 * h->shape.Hkv * h->shape.D;
 }
 
-// Replay forward of R suffix rows against the first P_eff rows of the handle's prefix.
-ls_status replay_fwd_impl(ls_prefix_t h, int64_t P_eff, int64_t R, const void* q,
-                          const void* k_suffix, const void* v_suffix, void* o, float* lse,
-                          void* stream) {
+// Packed-response offsets: 1 <= G <= kMaxPacked, cu[0] = 0, strictly increasing, total
+// below 2^31.
+ls_status check_cu(int32_t G, const int64_t* cu) {
+  if (cu == nullptr || G < 1) return LS_ERR_INVALID_ARGUMENT;
+  if (G > kMaxPacked) return LS_ERR_UNSUPPORTED;
+  if (cu[0] != 0) return LS_ERR_INVALID_ARGUMENT;
+  for (int b = 0; b < G; ++b)
+    if (cu[b + 1] <= cu[b]) return LS_ERR_INVALID_ARGUMENT;
+  if (cu[G] >= (int64_t(1) << 31)) return LS_ERR_UNSUPPORTED;
+  return LS_OK;
+}
+
+size_t bwd_workspace_bytes(ls_prefix_t h, int32_t G, const int64_t* cu) {
+  int64_t n_qt = 0;
+  for (int b = 0; b < G; ++b) n_qt += (cu[b + 1] - cu[b] + h->shape.qt - 1) / h->shape.qt;
+  return align_up(static_cast<size_t>(h->shape.Hkv) * n_qt * 256 * sizeof(float), 256);
+}
+
+// Replay forward of the packed responses cu (G of them, total rows cu[G]) against the first
+// P_eff rows of the handle's prefix.
+ls_status replay_fwd_impl(ls_prefix_t h, int64_t P_eff, int32_t G, const int64_t* cu,
+                          const void* q, const void* k_suffix, const void* v_suffix, void* o,
+                          float* lse, void* stream) {
   if (q == nullptr || k_suffix == nullptr || v_suffix == nullptr || o == nullptr ||
       lse == nullptr)
     return LS_ERR_INVALID_ARGUMENT;
-  if (R < 1) return LS_ERR_INVALID_ARGUMENT;
-  if (R >= (int64_t(1) << 31)) return LS_ERR_UNSUPPORTED;
+  ls_status st = check_cu(G, cu);
+  if (st != LS_OK) return st;
+  const int64_t R = cu[G];
   if (!aligned16(q) || !aligned16(k_suffix) || !aligned16(v_suffix) || !aligned16(o) ||
       !aligned_n(lse, 4))
     return LS_ERR_MISALIGNED;
   uint32_t* status = nullptr;
-  ls_status st = enter(h, stream, &status);
+  st = enter(h, stream, &status);
   if (st != LS_OK) return st;
 
   FwdArgs a{};
   a.sh = h->shape;
   a.sh.P = P_eff;
   a.sh.R = R;
+  varlen_build(&a.vl, G, cu, a.sh.qt);
   a.tm_kp = &h->tm_k;
   a.tm_vp = &h->tm_v;
   const AttnShape& sh = a.sh;
@@ -256,31 +277,35 @@ ls_status replay_fwd_impl(ls_prefix_t h, int64_t P_eff, int64_t R, const void* q
   return e == cudaSuccess ? LS_OK : cuda_fail(e, "replay forward launch");
 }
 
-// Replay backward against the first P_eff prefix rows.  suffix_to_acc: the suffix keys'
-// gradients go into the accumulators at rows P_eff + key (dk/dv_suffix unused).
-ls_status replay_bwd_impl(ls_prefix_t h, int64_t P_eff, int64_t R, const void* q,
-                          const void* k_suffix, const void* v_suffix, const void* o,
-                          const float* lse, const void* d_out, void* dq, void* dk_suffix,
-                          void* dv_suffix, int suffix_to_acc, void* workspace,
+// Replay backward of the packed responses against the first P_eff prefix rows.
+// suffix_to_acc (one response only): the suffix keys' gradients go into the accumulators at
+// rows P_eff + key (dk/dv_suffix unused).
+ls_status replay_bwd_impl(ls_prefix_t h, int64_t P_eff, int32_t G, const int64_t* cu,
+                          const void* q, const void* k_suffix, const void* v_suffix,
+                          const void* o, const float* lse, const void* d_out, void* dq,
+                          void* dk_suffix, void* dv_suffix, int suffix_to_acc, void* workspace,
                           size_t workspace_bytes, void* stream) {
   if (q == nullptr || k_suffix == nullptr || v_suffix == nullptr || o == nullptr ||
       lse == nullptr || d_out == nullptr || dq == nullptr)
     return LS_ERR_INVALID_ARGUMENT;
-  if (R < 1) return LS_ERR_INVALID_ARGUMENT;
-  if (R >= (int64_t(1) << 31)) return LS_ERR_UNSUPPORTED;
-  if (workspace == nullptr || workspace_bytes < ls_replay_bwd_workspace_bytes(h, R))
+  ls_status st = check_cu(G, cu);
+  if (st != LS_OK) return st;
+  if (suffix_to_acc && G != 1) return LS_ERR_INVALID_ARGUMENT;
+  const int64_t R = cu[G];
+  if (workspace == nullptr || workspace_bytes < bwd_workspace_bytes(h, G, cu))
     return LS_ERR_WORKSPACE;
   if (!aligned16(q) || !aligned16(k_suffix) || !aligned16(v_suffix) || !aligned16(o) ||
       !aligned16(d_out) || !aligned16(dq) || !aligned16(workspace) || !aligned_n(lse, 4))
     return LS_ERR_MISALIGNED;
   uint32_t* status = nullptr;
-  ls_status st = enter(h, stream, &status);
+  st = enter(h, stream, &status);
   if (st != LS_OK) return st;
 
   BwdArgs a{};
   a.sh = h->shape;
   a.sh.P = P_eff;
   a.sh.R = R;
+  varlen_build(&a.vl, G, cu, a.sh.qt);
   a.tm_kp = &h->tm_k;
   a.tm_vp = &h->tm_v;
   const AttnShape& sh = a.sh;
@@ -303,7 +328,7 @@ ls_status replay_bwd_impl(ls_prefix_t h, int64_t P_eff, int64_t R, const void* q
   {
     LaunchTimer t(LS_KERNEL_BWD_PREP, s);
     e = launch_bwd_prep(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(d_out), lse,
-                        rowstats, sh, s);
+                        rowstats, sh, a.vl, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "replay backward prep launch");
   {
@@ -447,7 +472,17 @@ ls_status ls_replay_fwd(ls_prefix_t h, int64_t R, const void* q, const void* k_s
                         const void* v_suffix, void* o, float* lse, void* stream) {
   ls_status st = check_handle(h);
   if (st != LS_OK) return st;
-  return replay_fwd_impl(h, h->shape.P, R, q, k_suffix, v_suffix, o, lse, stream);
+  const int64_t cu[2] = {0, R};
+  if (R < 1) return LS_ERR_INVALID_ARGUMENT;
+  return replay_fwd_impl(h, h->shape.P, 1, cu, q, k_suffix, v_suffix, o, lse, stream);
+}
+
+ls_status ls_replay_fwd_packed(ls_prefix_t h, int32_t G, const int64_t* cu_seqlens,
+                               const void* q, const void* k_suffix, const void* v_suffix,
+                               void* o, float* lse, void* stream) {
+  ls_status st = check_handle(h);
+  if (st != LS_OK) return st;
+  return replay_fwd_impl(h, h->shape.P, G, cu_seqlens, q, k_suffix, v_suffix, o, lse, stream);
 }
 
 ls_status ls_block_replay_fwd(ls_prefix_t h, int64_t prefix_len, int64_t R, const void* q,
@@ -455,14 +490,15 @@ ls_status ls_block_replay_fwd(ls_prefix_t h, int64_t prefix_len, int64_t R, cons
   ls_status st = check_handle(h);
   if (st != LS_OK) return st;
   if (prefix_len < 1 || R < 1 || prefix_len > h->shape.P - R) return LS_ERR_INVALID_ARGUMENT;
-  return replay_fwd_impl(h, prefix_len, R, q, block_rows(h, h->k_prefix, prefix_len),
+  const int64_t cu[2] = {0, R};
+  return replay_fwd_impl(h, prefix_len, 1, cu, q, block_rows(h, h->k_prefix, prefix_len),
                          block_rows(h, h->v_prefix, prefix_len), o, lse, stream);
 }
 
 size_t ls_replay_bwd_workspace_bytes(ls_prefix_t h, int64_t R) {
   if (check_handle(h) != LS_OK || R < 1) return 0;
-  const int64_t n_qt = (R + h->shape.qt - 1) / h->shape.qt;
-  return align_up(static_cast<size_t>(h->shape.Hkv) * n_qt * 256 * sizeof(float), 256);
+  const int64_t cu[2] = {0, R};
+  return bwd_workspace_bytes(h, 1, cu);
 }
 
 ls_status ls_replay_bwd(ls_prefix_t h, int64_t R, const void* q, const void* k_suffix,
@@ -473,8 +509,28 @@ ls_status ls_replay_bwd(ls_prefix_t h, int64_t R, const void* q, const void* k_s
   if (st != LS_OK) return st;
   if (dk_suffix == nullptr || dv_suffix == nullptr) return LS_ERR_INVALID_ARGUMENT;
   if (!aligned16(dk_suffix) || !aligned16(dv_suffix)) return LS_ERR_MISALIGNED;
-  return replay_bwd_impl(h, h->shape.P, R, q, k_suffix, v_suffix, o, lse, d_out, dq, dk_suffix,
-                         dv_suffix, 0, workspace, workspace_bytes, stream);
+  if (R < 1) return LS_ERR_INVALID_ARGUMENT;
+  const int64_t cu[2] = {0, R};
+  return replay_bwd_impl(h, h->shape.P, 1, cu, q, k_suffix, v_suffix, o, lse, d_out, dq,
+                         dk_suffix, dv_suffix, 0, workspace, workspace_bytes, stream);
+}
+
+size_t ls_replay_bwd_packed_workspace_bytes(ls_prefix_t h, int32_t G, const int64_t* cu_seqlens) {
+  if (check_handle(h) != LS_OK || check_cu(G, cu_seqlens) != LS_OK) return 0;
+  return bwd_workspace_bytes(h, G, cu_seqlens);
+}
+
+ls_status ls_replay_bwd_packed(ls_prefix_t h, int32_t G, const int64_t* cu_seqlens,
+                               const void* q, const void* k_suffix, const void* v_suffix,
+                               const void* o, const float* lse, const void* d_out, void* dq,
+                               void* dk_suffix, void* dv_suffix, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  ls_status st = check_handle(h);
+  if (st != LS_OK) return st;
+  if (dk_suffix == nullptr || dv_suffix == nullptr) return LS_ERR_INVALID_ARGUMENT;
+  if (!aligned16(dk_suffix) || !aligned16(dv_suffix)) return LS_ERR_MISALIGNED;
+  return replay_bwd_impl(h, h->shape.P, G, cu_seqlens, q, k_suffix, v_suffix, o, lse, d_out,
+                         dq, dk_suffix, dv_suffix, 0, workspace, workspace_bytes, stream);
 }
 
 ls_status ls_block_replay_bwd(ls_prefix_t h, int64_t prefix_len, int64_t R, const void* q,
@@ -483,7 +539,8 @@ ls_status ls_block_replay_bwd(ls_prefix_t h, int64_t prefix_len, int64_t R, cons
   ls_status st = check_handle(h);
   if (st != LS_OK) return st;
   if (prefix_len < 1 || R < 1 || prefix_len > h->shape.P - R) return LS_ERR_INVALID_ARGUMENT;
-  return replay_bwd_impl(h, prefix_len, R, q, block_rows(h, h->k_prefix, prefix_len),
+  const int64_t cu[2] = {0, R};
+  return replay_bwd_impl(h, prefix_len, 1, cu, q, block_rows(h, h->k_prefix, prefix_len),
                          block_rows(h, h->v_prefix, prefix_len), o, lse, d_out, dq, nullptr,
                          nullptr, 1, workspace, workspace_bytes, stream);
 }

@@ -43,8 +43,47 @@ struct AttnShape {
   int qt;        // queries per 128-row tile (= 128 / g)
 };
 
+// Responses packed along the token axis: response b owns packed rows row0[b] .. row0[b+1]-1
+// of Q/dO/O/dQ/LSE and of the suffix K/V, and sees the prompt and, causally, its own rows
+// only (the shared-prefix tree).  One response is the case G = 1.  The prefix sums count
+// each kernel's work units per response; a flat unit index maps to (response, local unit)
+// with varlen_find.
+constexpr int kMaxPacked = 64;
+struct Varlen {
+  int G;
+  int row0[kMaxPacked + 1];   // packed row offsets; row0[G] = total rows
+  int pair0[kMaxPacked + 1];  // forward units: pairs of 128-row Q tiles
+  int qt0[kMaxPacked + 1];    // 128-row Q tiles
+  int kt0[kMaxPacked + 1];    // 128-key suffix tiles
+};
+
+// The response b with pre[b] <= x < pre[b + 1] (pre non-decreasing, pre[0] = 0).
+__host__ __device__ inline int varlen_find(const int* pre, int G, int x) {
+  int lo = 0, hi = G - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pre[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Fill v for G responses of lengths cu[b+1] - cu[b] (all >= 1) and qt queries per tile.
+inline void varlen_build(Varlen* v, int G, const int64_t* cu, int qt) {
+  v->G = G;
+  v->row0[0] = v->pair0[0] = v->qt0[0] = v->kt0[0] = 0;
+  for (int b = 0; b < G; ++b) {
+    const int R = static_cast<int>(cu[b + 1] - cu[b]);
+    const int nq = (R + qt - 1) / qt;
+    v->row0[b + 1] = static_cast<int>(cu[b + 1]);
+    v->pair0[b + 1] = v->pair0[b] + (nq + 1) / 2;
+    v->qt0[b + 1] = v->qt0[b] + nq;
+    v->kt0[b + 1] = v->kt0[b] + (R + 127) / 128;
+  }
+}
+
 struct FwdArgs {
-  AttnShape sh;
+  AttnShape sh;               // sh.R = total packed rows
+  Varlen vl;
   const CUtensorMap* tm_kp;   // prompt K [P][Hkv][D] 3-D map, box {64, 1, 128}
   const CUtensorMap* tm_vp;
   CUtensorMap tm_q;           // Q [R][Hq][D], box {64, g, qt}
@@ -56,12 +95,13 @@ struct FwdArgs {
 cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t s);
 
 struct BwdArgs {
-  AttnShape sh;
+  AttnShape sh;               // sh.R = total packed rows
+  Varlen vl;
   const CUtensorMap* tm_kp;   // prompt K/V [P][Hkv][D], box {64, 1, 128}
   const CUtensorMap* tm_vp;
   CUtensorMap tm_q, tm_do;    // [R][Hq][D], box {64, g, qt}
   CUtensorMap tm_ks, tm_vs;   // suffix K/V [R][Hkv][D], box {64, 1, 128}
-  const float* rowstats;      // [Hkv][n_qt][256]: LSE log2 e of the tile's 128 rows, then Delta
+  const float* rowstats;      // [Hkv][qt0[G]][256]: LSE log2 e of a tile's 128 rows, then Delta
   uint16_t* dq;               // bf16 [R, Hq, D]
   uint16_t* dk_suf;           // bf16 [R, Hkv, D] (unused when suffix_to_acc)
   uint16_t* dv_suf;
@@ -70,11 +110,13 @@ struct BwdArgs {
   int suffix_to_acc;          // suffix key gradients are added into rows P + key of dk/dv_acc
   uint32_t* status;
 };
-// Row statistics of every 128-row Q tile slot (kv, i, r), r = (t - i qt) g + h - kv g:
-// valid rows get LSE log2 e and Delta = sum_d dO O; padding rows and rows past R get
-// (+inf, 0) so their softmax probabilities are exactly 0.
+// Row statistics of every 128-row Q tile slot (kv, f, r) -- f the flat tile index over the
+// packed responses, tile i = f - qt0[b] of response b, r = (t - i qt) g + h - kv g: valid
+// rows get LSE log2 e and Delta = sum_d dO O; padding rows and rows past the response's
+// end get (+inf, 0) so their softmax probabilities are exactly 0.
 cudaError_t launch_bwd_prep(const uint16_t* o, const uint16_t* d_out, const float* lse,
-                            float* rowstats, const AttnShape& sh, cudaStream_t s);
+                            float* rowstats, const AttnShape& sh, const Varlen& vl,
+                            cudaStream_t s);
 cudaError_t launch_attn_bwd_dkdv(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_attn_bwd_dq(const BwdArgs& a, cudaStream_t s);
 

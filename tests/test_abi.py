@@ -72,6 +72,10 @@ def test_calls_without_a_handle(L):
     assert L.ls_prefix_grad_finalize_rows(None, 0, 4, 1.0, None, None, 0, 0, None) == 3
     assert L.ls_block_replay_fwd(None, 16, 4, 0x1000, 0x1000, 0x1000, None) == 3
     assert L.ls_block_replay_bwd(None, 16, 4, *([0x1000] * 6), 1 << 20, None) == 3
+    cu = (ctypes.c_int64 * 3)(0, 2, 5)
+    assert L.ls_replay_fwd_packed(None, 2, cu, *([0x1000] * 5), None) == 3
+    assert L.ls_replay_bwd_packed(None, 2, cu, *([0x1000] * 10), 1 << 20, None) == 3
+    assert L.ls_replay_bwd_packed_workspace_bytes(None, 2, cu) == 0
     assert L.ls_replay_bwd_workspace_bytes(None, 4) == 0
     assert L.ls_prefix_destroy(None) == 0
 
