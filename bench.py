@@ -255,23 +255,38 @@ class Group:
         pre.close()
         torch.cuda.synchronize()
 
-    def inputs(self):
-        out = [self.kp, self.vp]
+    def input_groups(self):
+        """Device inputs of one step in the order a step consumes them: the prompt K/V, then
+        each response's tensors."""
+        out = [[self.kp, self.vp]]
         for r in self.resp:
-            out += [r["q"], r["ks"], r["vs"], r["do"], r["logits"], r["ids"], r["old"]]
+            out.append([r["q"], r["ks"], r["vs"], r["do"], r["logits"], r["ids"], r["old"]])
         return out
 
-    def step(self, loss_slot):
+    def step(self, loss_slot, ev_in=None, ev_used=None):
+        """One group step.  With events (end-to-end runs): input group k is waited for
+        (ev_in[k]) before its first use and ev_used[k] is recorded after its last use, so
+        the copies of later responses overlap the replay of earlier ones."""
+        import torch
         import long_context_grpo_gb300 as ls
         w = self.w
+        cur = torch.cuda.current_stream()
+        if ev_in is not None:
+            cur.wait_event(ev_in[0])
         pre = ls.Prefix(self.kp, self.vp, self.dk_acc, self.dv_acc, Hq=w.Hq)
         for i, (r, Ri) in enumerate(zip(self.resp, self.R)):
+            if ev_in is not None:
+                cur.wait_event(ev_in[1 + i])
             o, lse = pre.fwd(r["q"], r["ks"], r["vs"], o=self.o[:Ri], lse=self.lse[:Ri])
             ls.grpo_loss(r["logits"], r["ids"], r["old"], self.A[i], w.eps, w.G, loss_slot,
                          dlogits=self.dlog[:Ri], clip_mask=self.mask[:Ri],
                          logp_out=self.logp[:Ri], workspace=self.lws)
             pre.bwd(r["q"], r["ks"], r["vs"], o, lse, r["do"], dq=self.dq[:Ri],
                     dk_suffix=self.dks[:Ri], dv_suffix=self.dvs[:Ri], workspace=self.bws)
+            if ev_used is not None:
+                ev_used[1 + i].record(cur)
+        if ev_used is not None:
+            ev_used[0].record(cur)
         pre.finalize(1.0, self.dk_out, self.dv_out)
         pre.close()
 
@@ -546,36 +561,58 @@ def run_ours(args, w):
     # ---------------- end to end through the C ABI with host buffers
     e2e = None
     if not args.no_e2e:
-        dev_in = grp.inputs()
-        host_in = []
-        for t in dev_in:
-            h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-            h.copy_(t)
-            host_in.append(h)
-        h2d = sum(t.numel() * t.element_size() for t in host_in)
+        # Each step copies every input from pinned host memory: the prompt K/V first, then
+        # each response's tensors, on a copy stream, so that response i+1 is copied while
+        # response i is replayed; a buffer is overwritten only after its last use.
+        dev_groups = grp.input_groups()
+        host_groups = []
+        for g_ in dev_groups:
+            hg = []
+            for t in g_:
+                h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                h.copy_(t)
+                hg.append(h)
+            host_groups.append(hg)
+        h2d = sum(t.numel() * t.element_size() for hg in host_groups for t in hg)
         host_loss = torch.empty(1, dtype=torch.float64).pin_memory()
+        copy_stream = torch.cuda.Stream()
+        ev_in = [torch.cuda.Event() for _ in dev_groups]
+        ev_used = [torch.cuda.Event() for _ in dev_groups]
+        steps_done = [0]
 
         def e2e_step():
-            for h, d_ in zip(host_in, dev_in):
-                d_.copy_(h, non_blocking=True)
-            grp.step(losses[slot:slot + 1])
+            for k, (hg, dg) in enumerate(zip(host_groups, dev_groups)):
+                if steps_done[0] > 0:
+                    copy_stream.wait_event(ev_used[k])
+                with torch.cuda.stream(copy_stream):
+                    for h, d_ in zip(hg, dg):
+                        d_.copy_(h, non_blocking=True)
+                ev_in[k].record(copy_stream)
+            grp.step(losses[slot:slot + 1], ev_in=ev_in, ev_used=ev_used)
             host_loss.copy_(losses[slot:slot + 1], non_blocking=True)
+            steps_done[0] += 1
 
         e2e_step()   # untimed
         torch.cuda.synchronize()
         barrier()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
+        ls.timing_read()
+        ls.timing_enable(True)
         e0.record(stream)
+        copy_stream.wait_event(e0)
         for _ in range(args.steps):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
+        ls.timing_enable(False)
+        e2e_k = ls.timing_read()
         ems = max_over_ranks(e0.elapsed_time(e1))
         e2e = {"value": flops_all / (ems / 1e3) / 1e12, "unit": "TFLOP/s",
                "response_tok_s": toks_all / (ems / 1e3), "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": 8}
-        del host_in
+               "d2h_bytes_per_step": 8,
+               "kernel_ms_per_step": {k: round(v[0] / args.steps, 2) for k, v in e2e_k.items() if v[1] > 0}}
+        del host_groups
 
     # ---------------- CPU baseline (rank 0, N = 1 only)
     cpu = None
