@@ -14,6 +14,12 @@
  *     ls_replay_bwd            dQ, suffix dK/dV; prompt dK/dV added into the accumulators
  *   ls_prefix_grad_finalize    one finalization of the group-summed prompt gradient
  *
+ * Around that sequence: ls_token_logp (+ ls_replay_fwd) scores responses without
+ * gradients (old/reference policy); ls_block_replay_fwd/bwd replay one long response block
+ * by block (section 3-2 (4)); ls_replay_fwd_packed/bwd_packed replay a whole group in one
+ * launch per kernel; a handle may be kept across groups (prefix reuse, section 4-2) with
+ * ls_prefix_grad_finalize(..., reset_acc = 1) between them.
+ *
  * Conventions shared by every entry point
  *  - Pointers named "device" must point to device memory of the current CUDA device,
  *    allocated and owned by the caller.  The library allocates no device memory and never
