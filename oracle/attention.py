@@ -172,3 +172,20 @@ def response_rows(k_prefix, v_prefix, q, k_suffix, v_suffix, d_out, rows, scale=
             dS = Pm * (dP - (Pm * dP).sum())
             dq[idx] = s * (dS @ Kt)
     return o, lse, dq
+
+
+def merge_partials(o_parts, lse_parts):
+    """Combine attention results computed over disjoint key sets (one per prompt shard of a
+    context-parallel prompt; LongStraw review, section 3-2 (2): the cross-rank log-sum-exp
+    and output merge).  With lse_r = log sum_{j in K_r} exp(S_j) and o_r the softmax average
+    of the values over K_r, the attention over the union of the key sets is
+        lse = log sum_r exp(lse_r),   o = sum_r exp(lse_r - lse) o_r.
+    o_parts: list of [..., D]; lse_parts: list of [...] (natural log).  float64."""
+    lse_parts = [_f64(x) for x in lse_parts]
+    o_parts = [_f64(x) for x in o_parts]
+    m = np.max(np.stack(lse_parts), axis=0)
+    w = [np.exp(l - m) for l in lse_parts]
+    total = np.sum(np.stack(w), axis=0)
+    lse = m + np.log(total)
+    o = sum(wr[..., None] / total[..., None] * orr for wr, orr in zip(w, o_parts))
+    return o, lse

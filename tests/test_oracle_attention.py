@@ -196,3 +196,32 @@ def test_row_range_gives_exact_tail_key_gradients():
     np.testing.assert_allclose(part["dk_suffix"][6:], full["dk_suffix"][6:], rtol=1e-12, atol=1e-14)
     np.testing.assert_allclose(part["dv_suffix"][6:], full["dv_suffix"][6:], rtol=1e-12, atol=1e-14)
     assert np.all(part["o"][:6] == 0.0)
+
+
+def test_merge_of_key_shards_equals_attention_over_all_keys():
+    """Attention over a key set split into disjoint shards, each computed on its own by
+    torch (fp64 softmax and logsumexp), then merged by the oracle, equals torch's attention
+    over all keys; one part merges to itself; equal lse gives the plain average."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(21)
+    T, D, N = 7, 16, 53
+    q = torch.tensor(rng.normal(size=(T, D)))
+    k = torch.tensor(rng.normal(size=(N, D)) * 1.5)
+    v = torch.tensor(rng.normal(size=(N, D)))
+    s = q @ k.T / np.sqrt(D)
+    o_full = torch.softmax(s, dim=1) @ v
+    lse_full = torch.logsumexp(s, dim=1)
+    bounds = [0, 5, 6, 30, 53]
+    o_parts, lse_parts = [], []
+    for a, b in zip(bounds[:-1], bounds[1:]):
+        sp = s[:, a:b]
+        o_parts.append((torch.softmax(sp, dim=1) @ v[a:b]).numpy())
+        lse_parts.append(torch.logsumexp(sp, dim=1).numpy())
+    o, lse = att.merge_partials(o_parts, lse_parts)
+    assert np.allclose(o, o_full.numpy(), rtol=0, atol=1e-12)
+    assert np.allclose(lse, lse_full.numpy(), rtol=0, atol=1e-12)
+    o1, l1 = att.merge_partials(o_parts[:1], lse_parts[:1])
+    assert np.array_equal(o1, o_parts[0]) and np.allclose(l1, lse_parts[0], atol=0)
+    o2, l2 = att.merge_partials([o_parts[0], o_parts[1]], [lse_parts[0], lse_parts[0]])
+    assert np.allclose(o2, 0.5 * (o_parts[0] + o_parts[1]), atol=1e-15)
+    assert np.allclose(l2, lse_parts[0] + np.log(2.0), atol=1e-15)
