@@ -408,6 +408,63 @@ class Group:
                 "kernel_ms": {k: round(v[0], 3) for k, v in kt.items() if v[1] > 0},
                 "activation_bytes_held": extra}
 
+    def cp_replay(self, shards, stream):
+        """Context-parallel replay of the longest response with the prompt split into
+        `shards` contiguous shards (one handle each; the last also owns the causal suffix):
+        partial forwards, merge, shard backwards with the merged O/LSE, dQ part sum.  The
+        ranks are emulated on this GPU; timed after one untimed run."""
+        import torch
+        import long_context_grpo_gb300 as ls
+        w = self.w
+        i = max(range(len(self.R)), key=lambda k: self.R[k])
+        R, r = self.R[i], self.resp[i]
+        q, ks, vs, do = r["q"], r["ks"], r["vs"], r["do"]
+        bounds = [round(k * w.P / shards) for k in range(shards + 1)]
+        hs = [ls.Prefix(self.kp[a:b], self.vp[a:b], self.dk_acc[a:b], self.dv_acc[a:b], Hq=w.Hq)
+              for a, b in zip(bounds[:-1], bounds[1:])]
+        o_parts = [torch.empty_like(q) for _ in hs]
+        lse_parts = [torch.empty((R, w.Hq), dtype=torch.float32, device=q.device) for _ in hs]
+        dq_parts = [torch.empty_like(q) for _ in hs]
+        o, lse, dq = self.o[:R], self.lse[:R], self.dq[:R]
+
+        def run():
+            for h, op, lp in zip(hs[:-1], o_parts, lse_parts):
+                h.fwd_prompt_only(q, op, lp)
+            hs[-1].fwd(q, ks, vs, o=o_parts[-1], lse=lse_parts[-1])
+            ls.attn_merge(o_parts, lse_parts, o=o, lse=lse)
+            for h, dp in zip(hs[:-1], dq_parts):
+                h.bwd_prompt_only(q, o, lse, do, dq=dp, workspace=self.bws)
+            hs[-1].bwd(q, ks, vs, o, lse, do, dq=dq_parts[-1], dk_suffix=self.dks[:R],
+                       dv_suffix=self.dvs[:R], workspace=self.bws)
+            ls.sum_bf16(dq_parts, out=dq)
+
+        run()
+        torch.cuda.synchronize()
+        ls.timing_read()
+        ls.timing_enable(True)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ls.timing_enable(False)
+        kt = ls.timing_read()
+        for h in hs:
+            h.close()
+        ms = e0.elapsed_time(e1)
+        fl = 14 * w.D * w.Hq * pairs(w.P, R)
+        row = R * w.Hq
+        merge_bytes = shards * row * (2 * w.D + 4) + row * (2 * w.D + 4)
+        sum_bytes = (shards + 1) * row * 2 * w.D
+        mm, sm = kt["merge"][0], kt["sum"][0]
+        return {"shards": shards, "response_tokens": R, "ms": ms,
+                "tflops": fl / (ms / 1e3) / 1e12,
+                "merge_ms": mm, "merge_gbs": merge_bytes / (mm / 1e3) / 1e9 if mm > 0 else None,
+                "sum_ms": sm, "sum_gbs": sum_bytes / (sm / 1e3) / 1e9 if sm > 0 else None,
+                "note": "shards emulated as separate handles on one GPU; the collectives "
+                        "(all-gather of partials, reduce of dQ) are not run"}
+
     def flops(self):
         w = self.w
         return sum(14 * w.D * w.Hq * pairs(w.P, Ri) for Ri in self.R)
@@ -558,6 +615,11 @@ def run_ours(args, w):
         packed = grp.packed_replay(stream, losses[0:1])
         packed["vs_serial_step"] = packed["ms"] and (ms / args.steps) / packed["ms"]
 
+    # ---------------- context-parallel replay of the longest response (shards on this GPU)
+    cp = None
+    if args.cp_shards > 0 and rank == 0:
+        cp = grp.cp_replay(args.cp_shards, stream)
+
     # ---------------- end to end through the C ABI with host buffers
     e2e = None
     if not args.no_e2e:
@@ -647,6 +709,7 @@ def run_ours(args, w):
                 "scoring": score,
                 "block_replay": blk,
                 "packed_replay": packed,
+                "cp_replay": cp,
                 "receipt": {"gradient_semantics": "prompt dK/dV exposed (fp32, group-summed), "
                                                   "not propagated",
                             "residency": "prompt K/V resident in HBM for the group",
@@ -670,6 +733,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-score", action="store_true")
     ap.add_argument("--no-packed", action="store_true")
+    ap.add_argument("--cp-shards", type=int, default=8,
+                    help="prompt shards of the context-parallel measurement (0: skip it)")
     ap.add_argument("--block", type=int, default=4096,
                     help="block length of the blockwise-replay measurement (0: skip it)")
     args = ap.parse_args()

@@ -270,6 +270,41 @@ ls_status ls_grpo_loss_noalloc(int64_t R, int64_t V, int32_t G, const void* logi
 int64_t ls_grpo_loss_noalloc_max_rows(void);
 
 /*
+ * Context-parallel prompt sharding (LongStraw review, section 3-2 (2) "Physical page
+ * ownership": each rank owns a slice of the prompt's K/V pages; local attention results are
+ * combined by a cross-rank log-sum-exp and output merge).  Every shard is its own handle
+ * over its prompt rows; exactly one shard (the suffix owner) also sees the response's causal
+ * suffix and uses ls_replay_fwd/ls_replay_bwd, the others use the prompt-only calls below.
+ * Forward: every shard produces a partial (o_r, lse_r) for all R query rows, and
+ * ls_attn_merge combines them.  Backward: every shard runs with the MERGED o and lse (so its
+ * softmax probabilities are the global ones), adds the exact gradient of its own keys into
+ * its accumulators and returns its part of dq; ls_sum_bf16 adds the parts.  On several
+ * GPUs the merge inputs arrive by an all-gather and the dq parts leave by a reduce(-scatter);
+ * on one GPU the shards are separate handles and the calls below are the whole exchange.
+ *
+ * ls_replay_fwd_prompt_only / ls_replay_bwd_prompt_only: as ls_replay_fwd / ls_replay_bwd
+ * with the handle's prompt keys only (no suffix keys; no suffix gradients).  q, o, d_out,
+ * dq bf16 THD [R, Hq, D]; lse fp32 [R, Hq]; workspace as ls_replay_bwd_workspace_bytes.
+ *
+ * ls_attn_merge: lse[i] = log sum_r exp(lse_parts[r][i]);
+ *                o[i, :] = sum_r exp(lse_parts[r][i] - lse[i]) o_parts[r][i, :]
+ *   over the R * Hq rows; o_parts / lse_parts are HOST arrays of n device pointers (bf16
+ *   [R, Hq, D] / fp32 [R, Hq]); 1 <= n <= 16, D a multiple of 8 (else LS_ERR_UNSUPPORTED).
+ *   Weights and sums in fp32.
+ *
+ * ls_sum_bf16: out[i] = bf16(sum_r float(parts[r][i])), 0 <= i < count; parts a HOST array
+ *   of n device pointers (bf16); 1 <= n <= 16, count a multiple of 8.
+ */
+ls_status ls_replay_fwd_prompt_only(ls_prefix_t h, int64_t R, const void* q, void* o, float* lse,
+                                    void* stream);
+ls_status ls_replay_bwd_prompt_only(ls_prefix_t h, int64_t R, const void* q, const void* o,
+                                    const float* lse, const void* d_out, void* dq,
+                                    void* workspace, size_t workspace_bytes, void* stream);
+ls_status ls_attn_merge(int32_t n, int64_t R, int32_t Hq, int32_t D, const void* const* o_parts,
+                        const float* const* lse_parts, void* o, float* lse, void* stream);
+ls_status ls_sum_bf16(int32_t n, int64_t count, const void* const* parts, void* out, void* stream);
+
+/*
  * ls_prefix_grad_finalize -- the group's one finalization (review section 2-1 step 5;
  * section 3-2 (7)).  out = scale * acc for the prompt dK and dV accumulators.
  *   dk_out, dv_out  device [P, Hkv, D], bf16 (out_is_fp32 = 0) or fp32 (out_is_fp32 = 1);
@@ -315,7 +350,9 @@ typedef enum {
   LS_KERNEL_GRPO_LOSS = 5,     /* loss row pass + fixed-order reduction           */
   LS_KERNEL_FINALIZE = 6,      /* prompt-gradient finalization                    */
   LS_KERNEL_TOKEN_LOGP = 7,    /* scoring: token log-prob only                    */
-  LS_KERNEL_COUNT = 8
+  LS_KERNEL_MERGE = 8,         /* context-parallel partial-attention merge        */
+  LS_KERNEL_SUM = 9,           /* context-parallel dQ part sum                    */
+  LS_KERNEL_COUNT = 10
 } ls_kernel_id;
 
 ls_status ls_timing_enable(int enable);

@@ -65,6 +65,10 @@ def _load():
                                                         ctypes.c_int, ctypes.c_int, vp]),
         "ls_block_replay_fwd": (ctypes.c_int, [vp, i64, i64, vp, vp, vp, vp]),
         "ls_replay_fwd_packed": (ctypes.c_int, [vp, i32, vp, vp, vp, vp, vp, vp, vp]),
+        "ls_replay_fwd_prompt_only": (ctypes.c_int, [vp, i64, vp, vp, vp, vp]),
+        "ls_replay_bwd_prompt_only": (ctypes.c_int, [vp, i64, vp, vp, vp, vp, vp, vp, sz, vp]),
+        "ls_attn_merge": (ctypes.c_int, [i32, i64, i32, i32, vp, vp, vp, vp, vp]),
+        "ls_sum_bf16": (ctypes.c_int, [i32, i64, vp, vp, vp]),
         "ls_replay_bwd_packed_workspace_bytes": (sz, [vp, i32, vp]),
         "ls_replay_bwd_packed": (ctypes.c_int, [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                                 vp, sz, vp]),
@@ -244,6 +248,36 @@ class Prefix:
             "ls_replay_bwd_packed")
         return dq, dk_suffix, dv_suffix
 
+    def fwd_prompt_only(self, q, o=None, lse=None):
+        """Partial attention of q over this handle's prompt keys only (one prompt shard)."""
+        R = q.shape[0]
+        o = torch.empty_like(q) if o is None else o
+        if lse is None:
+            lse = torch.empty((R, self.Hq), dtype=torch.float32, device=q.device)
+        _check(_lib().ls_replay_fwd_prompt_only(
+            self._h, R, _ptr(q, "q", torch.bfloat16, (R, self.Hq, self.D)),
+            _ptr(o, "o", torch.bfloat16, (R, self.Hq, self.D)),
+            _ptr(lse, "lse", torch.float32, (R, self.Hq)), _stream()), "ls_replay_fwd_prompt_only")
+        return o, lse
+
+    def bwd_prompt_only(self, q, o, lse, d_out, dq=None, workspace=None):
+        """Backward over this handle's prompt keys only, with the merged (global) o and lse:
+        this shard's part of dq; its key/value gradients go into its accumulators."""
+        R = q.shape[0]
+        dq = torch.empty_like(q) if dq is None else dq
+        if workspace is None:
+            workspace = torch.empty(max(self.bwd_workspace_bytes(R), 16), dtype=torch.uint8,
+                                    device=q.device)
+        _check(_lib().ls_replay_bwd_prompt_only(
+            self._h, R, _ptr(q, "q", torch.bfloat16, (R, self.Hq, self.D)),
+            _ptr(o, "o", torch.bfloat16, (R, self.Hq, self.D)),
+            _ptr(lse, "lse", torch.float32, (R, self.Hq)),
+            _ptr(d_out, "d_out", torch.bfloat16, (R, self.Hq, self.D)),
+            _ptr(dq, "dq", torch.bfloat16, (R, self.Hq, self.D)),
+            _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream()),
+            "ls_replay_bwd_prompt_only")
+        return dq
+
     def block_fwd(self, prefix_len: int, q, o=None, lse=None):
         """Blockwise replay forward: the block's keys/values are rows prefix_len .. of the
         handle's K/V buffers; its queries see rows 0 .. prefix_len-1 and, causally, its own."""
@@ -297,6 +331,33 @@ class Prefix:
         return dk_out, dv_out
 
 
+def attn_merge(o_parts, lse_parts, o=None, lse=None):
+    """Merge per-shard partial attention results: lse = logsumexp_r lse_r,
+    o = sum_r exp(lse_r - lse) o_r (bf16 [R, Hq, D] parts, fp32 [R, Hq] lse)."""
+    n = len(o_parts)
+    R, Hq, D = o_parts[0].shape
+    o = torch.empty_like(o_parts[0]) if o is None else o
+    lse = torch.empty_like(lse_parts[0]) if lse is None else lse
+    op = (ctypes.c_void_p * n)(*[_ptr(t, "o_part", torch.bfloat16, (R, Hq, D)) for t in o_parts])
+    lp = (ctypes.c_void_p * n)(*[_ptr(t, "lse_part", torch.float32, (R, Hq)) for t in lse_parts])
+    _check(_lib().ls_attn_merge(n, R, Hq, D, ctypes.cast(op, ctypes.c_void_p),
+                                ctypes.cast(lp, ctypes.c_void_p),
+                                _ptr(o, "o", torch.bfloat16, (R, Hq, D)),
+                                _ptr(lse, "lse", torch.float32, (R, Hq)), _stream()), "ls_attn_merge")
+    return o, lse
+
+
+def sum_bf16(parts, out=None):
+    """out = bf16(sum of the bf16 parts), fp32 accumulation."""
+    n = len(parts)
+    out = torch.empty_like(parts[0]) if out is None else out
+    pp = (ctypes.c_void_p * n)(*[_ptr(t, "part", torch.bfloat16, tuple(parts[0].shape)) for t in parts])
+    _check(_lib().ls_sum_bf16(n, parts[0].numel(), ctypes.cast(pp, ctypes.c_void_p),
+                              _ptr(out, "out", torch.bfloat16, tuple(parts[0].shape)), _stream()),
+           "ls_sum_bf16")
+    return out
+
+
 def grpo_loss_workspace_bytes(R: int) -> int:
     return int(_lib().ls_grpo_loss_workspace_bytes(R))
 
@@ -324,7 +385,7 @@ def grpo_loss(logits, ids, logp_old, advantage: float, eps: float, G: int, loss_
 
 
 KERNEL_NAMES = ("zero", "replay_fwd", "bwd_prep", "bwd_dkdv", "bwd_dq", "grpo_loss", "finalize",
-                "token_logp")
+                "token_logp", "merge", "sum")
 
 
 def timing_enable(on: bool = True):

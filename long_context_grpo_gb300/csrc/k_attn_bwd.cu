@@ -90,13 +90,13 @@ struct KvUnit {
 // Flat unit u -> (kv head, 128-key tile).  A prompt tile is seen by every Q tile of every
 // packed response; a suffix tile of response b by that response's tiles from the first
 // one holding a query at or after its first key.
-template <bool kPacked>
+template <bool kPacked, bool kNoSuffix>
 __device__ __forceinline__ KvUnit make_kv_unit(int u, const AttnShape& sh, const Varlen& vl) {
   const int n_pt = static_cast<int>((sh.P + 127) / 128);
   KvUnit w;
   if constexpr (!kPacked) {
-    // one response: base 0, length sh.R
-    const int n_st = static_cast<int>((sh.R + 127) / 128);
+    // one response: base 0, length sh.R (kNoSuffix: prompt key tiles only)
+    const int n_st = kNoSuffix ? 0 : static_cast<int>((sh.R + 127) / 128);
     const int n_qt = static_cast<int>((sh.R + sh.qt - 1) / sh.qt);
     w.kv = u / (n_pt + n_st);
     const int j = u - w.kv * (n_pt + n_st);
@@ -132,7 +132,7 @@ __device__ __forceinline__ KvUnit make_kv_unit(int u, const AttnShape& sh, const
   return w;
 }
 
-template <int D, bool kPacked>
+template <int D, bool kPacked, bool kNoSuffix>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_kp,
                          const __grid_constant__ CUtensorMap tm_vp,
@@ -155,7 +155,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_qt = kPacked ? vl.qt0[vl.G] : static_cast<int>((sh.R + sh.qt - 1) / sh.qt);
   const int n_units = sh.Hkv * (static_cast<int>((sh.P + 127) / 128) +
-                                (kPacked ? vl.kt0[vl.G] : static_cast<int>((sh.R + 127) / 128)));
+                                (kPacked ? vl.kt0[vl.G]
+                                         : (kNoSuffix ? 0 : static_cast<int>((sh.R + 127) / 128))));
   const int rows_used = sh.g * sh.qt;   // rows of a 128-row tile that TMA fills
 
   // Padding rows of every Q/dO buffer are never written by TMA: zero them once so that
@@ -219,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t qit = 0, uc = 0;
       bool ok = true, kv_pending = false;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
-        const KvUnit w = make_kv_unit<kPacked>(u, sh, vl);
+        const KvUnit w = make_kv_unit<kPacked, kNoSuffix>(u, sh, vl);
         if (uc > 0) ok = mbar_wait(&bars[C::kBarKVEmpty], (uc - 1) & 1u, status, vabort);
         if (!ok) break;
         mbar_arrive_expect_tx(&bars[C::kBarKVFull], 2 * C::kTile);
@@ -323,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&bars[C::kBarOEmpty + it % C::kNO]);
       };
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
-        const KvUnit w = make_kv_unit<kPacked>(u, sh, vl);
+        const KvUnit w = make_kv_unit<kPacked, kNoSuffix>(u, sh, vl);
         ok = mbar_wait(&bars[C::kBarKVFull], uc & 1u, status, vabort);
         if (!ok) break;
         tc_fence_after();
@@ -365,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t qit = 0u, uc = 0u, n_tiles = 0u;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
-      const KvUnit w = make_kv_unit<kPacked>(u, sh, vl);
+      const KvUnit w = make_kv_unit<kPacked, kNoSuffix>(u, sh, vl);
       const int key = w.key0 + row;
       for (int li = 0; li < w.n; ++li, ++n_tiles) {
         // row statistics of this Q tile: every thread reads the same 1 KB (L1 broadcast)
@@ -576,13 +577,18 @@ __device__ __forceinline__ QUnit make_q_unit_packed(int u, const AttnShape& sh, 
   return w;
 }
 
-template <bool kPacked>
+template <bool kPacked, bool kNoSuffix>
 __device__ __forceinline__ QUnit pick_q_unit(int u, const AttnShape& sh, int n_qt, const Varlen& vl) {
-  if constexpr (kPacked) return make_q_unit_packed(u, sh, vl);
-  else return make_q_unit(u, sh, n_qt);
+  if constexpr (kPacked) {
+    return make_q_unit_packed(u, sh, vl);
+  } else {
+    QUnit w = make_q_unit(u, sh, n_qt);
+    if constexpr (kNoSuffix) w.n = w.n_pt;
+    return w;
+  }
 }
 
-template <int D, bool kPacked>
+template <int D, bool kPacked, bool kNoSuffix>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_kp,
                        const __grid_constant__ CUtensorMap tm_vp,
@@ -649,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t kit = 0, uc = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
-        const QUnit w = pick_q_unit<kPacked>(u, sh, n_qt, vl);
+        const QUnit w = pick_q_unit<kPacked, kNoSuffix>(u, sh, n_qt, vl);
         if (uc > 0) ok = mbar_wait(&bars[C::kBarQEmpty], (uc - 1) & 1u, status, vabort);
         if (!ok) break;
         mbar_arrive_expect_tx(&bars[C::kBarQFull],
@@ -743,7 +749,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&bars[C::kBarKEmpty + sk]);
       };
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
-        const QUnit w = pick_q_unit<kPacked>(u, sh, n_qt, vl);
+        const QUnit w = pick_q_unit<kPacked, kNoSuffix>(u, sh, n_qt, vl);
         ok = mbar_wait(&bars[C::kBarQTmem], uc & 1u, status, vabort);
         if (!ok) break;
         tc_fence_after();
@@ -784,7 +790,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t uc = 0u, n_steps = 0u;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
-      const QUnit w = pick_q_unit<kPacked>(u, sh, n_qt, vl);
+      const QUnit w = pick_q_unit<kPacked, kNoSuffix>(u, sh, n_qt, vl);
       const int t = w.t0 + row / sh.g;
       const int hg = row % sh.g;
       const bool valid = (row < sh.g * sh.qt) && (kPacked ? t < w.R : t < sh.R);
@@ -917,32 +923,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool kPacked>
+template <int D, bool kPacked, bool kNoSuffix = false>
 cudaError_t launch_dkdv_d(const BwdArgs& a, cudaStream_t s) {
   using C = DkdvCfg<D>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D, kPacked>,
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D, kPacked, kNoSuffix>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   const int64_t n_units =
-      static_cast<int64_t>(a.sh.Hkv) * ((a.sh.P + 127) / 128 + a.vl.kt0[a.vl.G]);
+      static_cast<int64_t>(a.sh.Hkv) * ((a.sh.P + 127) / 128 + (kNoSuffix ? 0 : a.vl.kt0[a.vl.G]));
   int grid = num_sms();
   if (n_units < grid) grid = static_cast<int>(n_units);
-  attn_bwd_dkdv_kernel<D, kPacked><<<grid, kThreads, C::kSmem, s>>>(
+  attn_bwd_dkdv_kernel<D, kPacked, kNoSuffix><<<grid, kThreads, C::kSmem, s>>>(
       *a.tm_kp, *a.tm_vp, a.tm_ks, a.tm_vs, a.tm_q, a.tm_do, a.sh, a.rowstats, a.dk_acc,
       a.dv_acc, a.dk_suf, a.dv_suf, a.suffix_to_acc, a.vl, a.status);
   return cudaGetLastError();
 }
 
-template <int D, bool kPacked>
+template <int D, bool kPacked, bool kNoSuffix = false>
 cudaError_t launch_dq_d(const BwdArgs& a, cudaStream_t s) {
   using C = DqCfg<D>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_dq_kernel<D, kPacked>,
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_dq_kernel<D, kPacked, kNoSuffix>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
@@ -950,7 +956,7 @@ cudaError_t launch_dq_d(const BwdArgs& a, cudaStream_t s) {
   const int64_t n_units = static_cast<int64_t>(a.sh.Hkv) * a.vl.qt0[a.vl.G];
   int grid = num_sms();
   if (n_units < grid) grid = static_cast<int>(n_units);
-  attn_bwd_dq_kernel<D, kPacked><<<grid, kThreads, C::kSmem, s>>>(*a.tm_kp, *a.tm_vp, a.tm_ks, a.tm_vs,
+  attn_bwd_dq_kernel<D, kPacked, kNoSuffix><<<grid, kThreads, C::kSmem, s>>>(*a.tm_kp, *a.tm_vp, a.tm_ks, a.tm_vs,
                                                         a.tm_q, a.tm_do, a.sh, a.rowstats, a.dq,
                                                         a.vl, a.status);
   return cudaGetLastError();
@@ -959,11 +965,13 @@ cudaError_t launch_dq_d(const BwdArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_attn_bwd_dkdv(const BwdArgs& a, cudaStream_t s) {
+  if (a.no_suffix) return a.sh.D == 128 ? launch_dkdv_d<128, false, true>(a, s) : launch_dkdv_d<64, false, true>(a, s);
   if (a.vl.G > 1) return a.sh.D == 128 ? launch_dkdv_d<128, true>(a, s) : launch_dkdv_d<64, true>(a, s);
   return a.sh.D == 128 ? launch_dkdv_d<128, false>(a, s) : launch_dkdv_d<64, false>(a, s);
 }
 
 cudaError_t launch_attn_bwd_dq(const BwdArgs& a, cudaStream_t s) {
+  if (a.no_suffix) return a.sh.D == 128 ? launch_dq_d<128, false, true>(a, s) : launch_dq_d<64, false, true>(a, s);
   if (a.vl.G > 1) return a.sh.D == 128 ? launch_dq_d<128, true>(a, s) : launch_dq_d<64, true>(a, s);
   return a.sh.D == 128 ? launch_dq_d<128, false>(a, s) : launch_dq_d<64, false>(a, s);
 }

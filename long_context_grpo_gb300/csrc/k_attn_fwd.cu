@@ -107,13 +107,19 @@ __device__ __forceinline__ Unit make_unit_packed(int u, const AttnShape& sh, con
   return w;
 }
 
-template <bool kPacked>
+// kNoSuffix: the queries see the prompt keys only (one shard of a context-parallel prompt).
+template <bool kPacked, bool kNoSuffix>
 __device__ __forceinline__ Unit pick_unit(int u, const AttnShape& sh, int n_pairs, const Varlen& vl) {
-  if constexpr (kPacked) return make_unit_packed(u, sh, vl);
-  else return make_unit(u, sh, n_pairs);
+  if constexpr (kPacked) {
+    return make_unit_packed(u, sh, vl);
+  } else {
+    Unit w = make_unit(u, sh, n_pairs);
+    if constexpr (kNoSuffix) w.n_kt = w.n_pt;
+    return w;
+  }
 }
 
-template <int D, bool kPacked>
+template <int D, bool kPacked, bool kNoSuffix>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_kp,
                     const __grid_constant__ CUtensorMap tm_vp,
@@ -179,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t kit = 0, vit = 0, uc = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
-        const Unit w = pick_unit<kPacked>(u, sh, n_pairs, vl);
+        const Unit w = pick_unit<kPacked, kNoSuffix>(u, sh, n_pairs, vl);
         if (uc > 0) ok = mbar_wait(&bars[C::kBarQEmpty], (uc - 1) & 1u, status);
         if (!ok) break;
         const int nq = w.has1 ? 2 : 1;
@@ -264,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
 
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
-        const Unit w = pick_unit<kPacked>(u, sh, n_pairs, vl);
+        const Unit w = pick_unit<kPacked, kNoSuffix>(u, sh, n_pairs, vl);
         const int nq = w.has1 ? 2 : 1;
         ok = mbar_wait(&bars[C::kBarQFull], uc & 1u, status, vabort);
         if (!ok) break;
@@ -337,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t sph = 0u, uq = 0u;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-      const Unit w = pick_unit<kPacked>(u, sh, n_pairs, vl);
+      const Unit w = pick_unit<kPacked, kNoSuffix>(u, sh, n_pairs, vl);
       if (q == 1 && !w.has1) continue;
       const int t = w.t0 + q * sh.qt + row / sh.g;
       float m_run = -INFINITY, l = 0.0f;
@@ -459,12 +465,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool kPacked>
+template <int D, bool kPacked, bool kNoSuffix = false>
 cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t s) {
   using C = FwdCfg<D>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, kPacked>,
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, kPacked, kNoSuffix>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
@@ -472,7 +478,7 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t s) {
   const int64_t n_units = static_cast<int64_t>(a.sh.Hkv) * a.vl.pair0[a.vl.G];
   int grid = num_sms();
   if (n_units < grid) grid = static_cast<int>(n_units);
-  attn_fwd_kernel<D, kPacked><<<grid, kThreads, C::kSmem, s>>>(
+  attn_fwd_kernel<D, kPacked, kNoSuffix><<<grid, kThreads, C::kSmem, s>>>(
       *a.tm_kp, *a.tm_vp, a.tm_q, a.tm_ks, a.tm_vs, a.sh, a.vl, a.o, a.lse, a.status);
   return cudaGetLastError();
 }
@@ -480,6 +486,7 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t s) {
+  if (a.no_suffix) return a.sh.D == 128 ? launch_fwd_d<128, false, true>(a, s) : launch_fwd_d<64, false, true>(a, s);
   if (a.vl.G > 1) return a.sh.D == 128 ? launch_fwd_d<128, true>(a, s) : launch_fwd_d<64, true>(a, s);
   return a.sh.D == 128 ? launch_fwd_d<128, false>(a, s) : launch_fwd_d<64, false>(a, s);
 }

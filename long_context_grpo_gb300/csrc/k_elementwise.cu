@@ -4,6 +4,10 @@
 //                      one finalization (LongStraw review, section 2-1 step 5)
 //   K2 bwd_prep        Delta[t,h] = sum_d dO[t,h,d] O[t,h,d], the row term of the softmax
 //                      backward dS = P * (dP - Delta), packed with LSE by 128-row Q tile
+//   merge              context-parallel combination of per-shard partial attention results:
+//                      lse = log sum_r exp(lse_r), o = sum_r exp(lse_r - lse) o_r
+//                      (LongStraw review, section 3-2 (2): global LSE/output merge)
+//   sum_bf16           sum of per-shard dQ partials, fp32 accumulation, bf16 out
 // All use 128-bit accesses on a grid sized to the SM count.
 #include "ls_internal.h"
 #include "ptx.cuh"
@@ -101,6 +105,67 @@ __global__ void __launch_bounds__(kThreads) bwd_prep_kernel(const uint4* o, cons
   }
 }
 
+// One thread per (row, 8 output values).  The shard weights exp(lse_r - m) are recomputed
+// per shard instead of kept in an array, so nothing is indexed dynamically.
+__global__ void __launch_bounds__(kThreads) attn_merge_kernel(const __grid_constant__ MergeArgs a) {
+  const int per_row = a.D / 8;
+  const int64_t total = a.rows * per_row;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x; idx < total;
+       idx += stride) {
+    const int64_t row = idx / per_row;
+    const int c = static_cast<int>(idx - row * per_row);
+    float m = -INFINITY;
+    for (int r = 0; r < a.n; ++r) m = fmaxf(m, a.lse_parts[r][row]);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float ssum = 0.f;
+    if (m != -INFINITY) {
+      for (int r = 0; r < a.n; ++r) ssum += expf(a.lse_parts[r][row] - m);
+      const float inv = 1.0f / ssum;
+      for (int r = 0; r < a.n; ++r) {
+        const float wr = expf(a.lse_parts[r][row] - m) * inv;
+        const uint4 v = __ldcs(reinterpret_cast<const uint4*>(a.o_parts[r] + row * a.D) + c);
+        const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          acc[2 * k] = fmaf(wr, __uint_as_float(vw[k] << 16), acc[2 * k]);
+          acc[2 * k + 1] = fmaf(wr, __uint_as_float(vw[k] & 0xFFFF0000u), acc[2 * k + 1]);
+        }
+      }
+    }
+    uint4 o;
+    o.x = bf16x2_rn(acc[0], acc[1]);
+    o.y = bf16x2_rn(acc[2], acc[3]);
+    o.z = bf16x2_rn(acc[4], acc[5]);
+    o.w = bf16x2_rn(acc[6], acc[7]);
+    __stcs(reinterpret_cast<uint4*>(a.o + row * a.D) + c, o);
+    if (c == 0) a.lse[row] = (m == -INFINITY) ? -INFINITY : m + logf(ssum);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) sum_bf16_kernel(const __grid_constant__ SumArgs a) {
+  const int64_t n8 = a.count / 8;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x; i < n8; i += stride) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int r = 0; r < a.n; ++r) {
+      const uint4 v = __ldcs(reinterpret_cast<const uint4*>(a.parts[r]) + i);
+      const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        acc[2 * k] += __uint_as_float(vw[k] << 16);
+        acc[2 * k + 1] += __uint_as_float(vw[k] & 0xFFFF0000u);
+      }
+    }
+    uint4 o;
+    o.x = bf16x2_rn(acc[0], acc[1]);
+    o.y = bf16x2_rn(acc[2], acc[3]);
+    o.z = bf16x2_rn(acc[4], acc[5]);
+    o.w = bf16x2_rn(acc[6], acc[7]);
+    __stcs(reinterpret_cast<uint4*>(a.out) + i, o);
+  }
+}
+
 // Failure-detection self test: one thread waits on an mbarrier that nothing arrives at,
 // bounded by limit_ns, then records DEV_WAIT_TIMEOUT exactly as the replay kernels do when
 // a wait gives up, and exits; the context stays usable.
@@ -151,6 +216,16 @@ cudaError_t launch_scale_inplace(float* acc, size_t n, float scale, cudaStream_t
 
 cudaError_t launch_wait_timeout(uint64_t limit_ns, uint32_t* status, cudaStream_t s) {
   wait_timeout_kernel<<<1, 32, 0, s>>>(limit_ns, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_merge(const MergeArgs& a, cudaStream_t s) {
+  attn_merge_kernel<<<grid_for(static_cast<size_t>(a.rows) * (a.D / 8)), kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sum_bf16(const SumArgs& a, cudaStream_t s) {
+  sum_bf16_kernel<<<grid_for(static_cast<size_t>(a.count / 8)), kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

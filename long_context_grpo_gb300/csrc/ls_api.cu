@@ -240,7 +240,7 @@ size_t bwd_workspace_bytes(ls_prefix_t h, int32_t G, const int64_t* cu) {
 // P_eff rows of the handle's prefix.
 ls_status replay_fwd_impl(ls_prefix_t h, int64_t P_eff, int32_t G, const int64_t* cu,
                           const void* q, const void* k_suffix, const void* v_suffix, void* o,
-                          float* lse, void* stream) {
+                          float* lse, void* stream, int no_suffix = 0) {
   if (q == nullptr || k_suffix == nullptr || v_suffix == nullptr || o == nullptr ||
       lse == nullptr)
     return LS_ERR_INVALID_ARGUMENT;
@@ -263,11 +263,17 @@ ls_status replay_fwd_impl(ls_prefix_t h, int64_t P_eff, int32_t G, const int64_t
   a.tm_vp = &h->tm_v;
   const AttnShape& sh = a.sh;
   st = encode_thd(&a.tm_q, q, R, sh.Hq, sh.D, sh.g, sh.qt);
-  if (st == LS_OK) st = encode_thd(&a.tm_ks, k_suffix, R, sh.Hkv, sh.D, 1, 128);
-  if (st == LS_OK) st = encode_thd(&a.tm_vs, v_suffix, R, sh.Hkv, sh.D, 1, 128);
+  if (no_suffix) {
+    a.tm_ks = h->tm_k;   // never read: prompt keys only
+    a.tm_vs = h->tm_v;
+  } else {
+    if (st == LS_OK) st = encode_thd(&a.tm_ks, k_suffix, R, sh.Hkv, sh.D, 1, 128);
+    if (st == LS_OK) st = encode_thd(&a.tm_vs, v_suffix, R, sh.Hkv, sh.D, 1, 128);
+  }
   if (st != LS_OK) return st;
   a.o = static_cast<uint16_t*>(o);
   a.lse = lse;
+  a.no_suffix = no_suffix;
   a.status = status;
   cudaError_t e;
   {
@@ -284,7 +290,7 @@ ls_status replay_bwd_impl(ls_prefix_t h, int64_t P_eff, int32_t G, const int64_t
                           const void* q, const void* k_suffix, const void* v_suffix,
                           const void* o, const float* lse, const void* d_out, void* dq,
                           void* dk_suffix, void* dv_suffix, int suffix_to_acc, void* workspace,
-                          size_t workspace_bytes, void* stream) {
+                          size_t workspace_bytes, void* stream, int no_suffix = 0) {
   if (q == nullptr || k_suffix == nullptr || v_suffix == nullptr || o == nullptr ||
       lse == nullptr || d_out == nullptr || dq == nullptr)
     return LS_ERR_INVALID_ARGUMENT;
@@ -311,8 +317,13 @@ ls_status replay_bwd_impl(ls_prefix_t h, int64_t P_eff, int32_t G, const int64_t
   const AttnShape& sh = a.sh;
   st = encode_thd(&a.tm_q, q, R, sh.Hq, sh.D, sh.g, sh.qt);
   if (st == LS_OK) st = encode_thd(&a.tm_do, d_out, R, sh.Hq, sh.D, sh.g, sh.qt);
-  if (st == LS_OK) st = encode_thd(&a.tm_ks, k_suffix, R, sh.Hkv, sh.D, 1, 128);
-  if (st == LS_OK) st = encode_thd(&a.tm_vs, v_suffix, R, sh.Hkv, sh.D, 1, 128);
+  if (no_suffix) {
+    a.tm_ks = h->tm_k;   // never read: prompt keys only
+    a.tm_vs = h->tm_v;
+  } else {
+    if (st == LS_OK) st = encode_thd(&a.tm_ks, k_suffix, R, sh.Hkv, sh.D, 1, 128);
+    if (st == LS_OK) st = encode_thd(&a.tm_vs, v_suffix, R, sh.Hkv, sh.D, 1, 128);
+  }
   if (st != LS_OK) return st;
   float* rowstats = static_cast<float*>(workspace);
   a.rowstats = rowstats;
@@ -322,6 +333,7 @@ ls_status replay_bwd_impl(ls_prefix_t h, int64_t P_eff, int32_t G, const int64_t
   a.dk_acc = h->dk_acc;
   a.dv_acc = h->dv_acc;
   a.suffix_to_acc = suffix_to_acc;
+  a.no_suffix = no_suffix;
   a.status = status;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
@@ -616,6 +628,80 @@ ls_status ls_token_logp(int64_t R, int64_t V, const void* logits, const int32_t*
     e = launch_token_logp(a, static_cast<cudaStream_t>(stream));
   }
   return e == cudaSuccess ? LS_OK : cuda_fail(e, "token log-prob launch");
+}
+
+ls_status ls_replay_fwd_prompt_only(ls_prefix_t h, int64_t R, const void* q, void* o, float* lse,
+                                    void* stream) {
+  ls_status st = check_handle(h);
+  if (st != LS_OK) return st;
+  if (R < 1) return LS_ERR_INVALID_ARGUMENT;
+  const int64_t cu[2] = {0, R};
+  return replay_fwd_impl(h, h->shape.P, 1, cu, q, h->k_prefix, h->v_prefix, o, lse, stream, 1);
+}
+
+ls_status ls_replay_bwd_prompt_only(ls_prefix_t h, int64_t R, const void* q, const void* o,
+                                    const float* lse, const void* d_out, void* dq,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+  ls_status st = check_handle(h);
+  if (st != LS_OK) return st;
+  if (R < 1) return LS_ERR_INVALID_ARGUMENT;
+  const int64_t cu[2] = {0, R};
+  return replay_bwd_impl(h, h->shape.P, 1, cu, q, h->k_prefix, h->v_prefix, o, lse, d_out, dq,
+                         nullptr, nullptr, 0, workspace, workspace_bytes, stream, 1);
+}
+
+ls_status ls_attn_merge(int32_t n, int64_t R, int32_t Hq, int32_t D, const void* const* o_parts,
+                        const float* const* lse_parts, void* o, float* lse, void* stream) {
+  if (o_parts == nullptr || lse_parts == nullptr || o == nullptr || lse == nullptr)
+    return LS_ERR_INVALID_ARGUMENT;
+  if (n < 1 || R < 1 || Hq < 1 || D < 8) return LS_ERR_INVALID_ARGUMENT;
+  if (n > kMaxParts || D % 8 != 0) return LS_ERR_UNSUPPORTED;
+  MergeArgs a{};
+  a.n = n;
+  a.rows = R * Hq;
+  a.D = D;
+  for (int r = 0; r < n; ++r) {
+    if (o_parts[r] == nullptr || lse_parts[r] == nullptr) return LS_ERR_INVALID_ARGUMENT;
+    if (!aligned16(o_parts[r]) || !aligned_n(lse_parts[r], 4)) return LS_ERR_MISALIGNED;
+    a.o_parts[r] = static_cast<const uint16_t*>(o_parts[r]);
+    a.lse_parts[r] = lse_parts[r];
+  }
+  if (!aligned16(o) || !aligned_n(lse, 4)) return LS_ERR_MISALIGNED;
+  a.o = static_cast<uint16_t*>(o);
+  a.lse = lse;
+  uint32_t* status = nullptr;
+  ls_status st = enter(nullptr, stream, &status);
+  if (st != LS_OK) return st;
+  cudaError_t e;
+  {
+    LaunchTimer t(LS_KERNEL_MERGE, static_cast<cudaStream_t>(stream));
+    e = launch_attn_merge(a, static_cast<cudaStream_t>(stream));
+  }
+  return e == cudaSuccess ? LS_OK : cuda_fail(e, "merge launch");
+}
+
+ls_status ls_sum_bf16(int32_t n, int64_t count, const void* const* parts, void* out, void* stream) {
+  if (parts == nullptr || out == nullptr || n < 1 || count < 1) return LS_ERR_INVALID_ARGUMENT;
+  if (n > kMaxParts || count % 8 != 0) return LS_ERR_UNSUPPORTED;
+  SumArgs a{};
+  a.n = n;
+  a.count = count;
+  for (int r = 0; r < n; ++r) {
+    if (parts[r] == nullptr) return LS_ERR_INVALID_ARGUMENT;
+    if (!aligned16(parts[r])) return LS_ERR_MISALIGNED;
+    a.parts[r] = static_cast<const uint16_t*>(parts[r]);
+  }
+  if (!aligned16(out)) return LS_ERR_MISALIGNED;
+  a.out = static_cast<uint16_t*>(out);
+  uint32_t* status = nullptr;
+  ls_status st = enter(nullptr, stream, &status);
+  if (st != LS_OK) return st;
+  cudaError_t e;
+  {
+    LaunchTimer t(LS_KERNEL_SUM, static_cast<cudaStream_t>(stream));
+    e = launch_sum_bf16(a, static_cast<cudaStream_t>(stream));
+  }
+  return e == cudaSuccess ? LS_OK : cuda_fail(e, "sum launch");
 }
 
 ls_status ls_prefix_grad_finalize(ls_prefix_t h, float scale, void* dk_out, void* dv_out,

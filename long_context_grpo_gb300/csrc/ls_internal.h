@@ -33,6 +33,27 @@ cudaError_t launch_zero_f32(float* p, size_t n, cudaStream_t s);
 cudaError_t launch_finalize(const float* acc, void* out, size_t n, float scale, int out_fp32,
                             int reset, cudaStream_t s);
 cudaError_t launch_wait_timeout(uint64_t limit_ns, uint32_t* status, cudaStream_t s);
+// Context-parallel merge of n partial attention results (one per prompt shard) of rows x
+// heads rows of D values: lse = log sum_r exp(lse_r), o = sum_r exp(lse_r - lse) o_r.
+constexpr int kMaxParts = 16;
+struct MergeArgs {
+  int n;
+  int64_t rows;               // R * Hq
+  int D;
+  const uint16_t* o_parts[kMaxParts];
+  const float* lse_parts[kMaxParts];
+  uint16_t* o;
+  float* lse;
+};
+cudaError_t launch_attn_merge(const MergeArgs& a, cudaStream_t s);
+// out = bf16(sum_r float(parts_r)) over count elements (count a multiple of 8).
+struct SumArgs {
+  int n;
+  int64_t count;
+  const uint16_t* parts[kMaxParts];
+  uint16_t* out;
+};
+cudaError_t launch_sum_bf16(const SumArgs& a, cudaStream_t s);
 cudaError_t launch_scale_inplace(float* acc, size_t n, float scale, cudaStream_t s);
 
 // ----- attention (k_attn_fwd.cu, k_attn_bwd.cu)
@@ -90,6 +111,7 @@ struct FwdArgs {
   CUtensorMap tm_ks, tm_vs;   // suffix K/V [R][Hkv][D], box {64, 1, 128}
   uint16_t* o;
   float* lse;
+  int no_suffix;              // 1: prompt keys only (one shard of a context-parallel prompt)
   uint32_t* status;
 };
 cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t s);
@@ -108,6 +130,7 @@ struct BwdArgs {
   float* dk_acc;              // fp32 [P, Hkv, D] (rows P .. P+R-1 too when suffix_to_acc)
   float* dv_acc;
   int suffix_to_acc;          // suffix key gradients are added into rows P + key of dk/dv_acc
+  int no_suffix;              // 1: prompt keys only (one shard of a context-parallel prompt)
   uint32_t* status;
 };
 // Row statistics of every 128-row Q tile slot (kv, f, r) -- f the flat tile index over the

@@ -76,6 +76,21 @@ def test_calls_without_a_handle(L):
     assert L.ls_replay_fwd_packed(None, 2, cu, *([0x1000] * 5), None) == 3
     assert L.ls_replay_bwd_packed(None, 2, cu, *([0x1000] * 10), 1 << 20, None) == 3
     assert L.ls_replay_bwd_packed_workspace_bytes(None, 2, cu) == 0
+    assert L.ls_replay_fwd_prompt_only(None, 4, 0x1000, 0x1000, 0x1000, None) == 3
+    assert L.ls_replay_bwd_prompt_only(None, 4, *([0x1000] * 6), 1 << 20, None) == 3
+
+
+def test_merge_and_sum_argument_checks(L):
+    parts = (ctypes.c_void_p * 2)(0x1000, 0x2000)
+    lses = (ctypes.c_void_p * 2)(0x3000, 0x4000)
+    assert L.ls_attn_merge(0, 4, 2, 64, parts, lses, 0x5000, 0x6000, None) == 1     # n < 1
+    assert L.ls_attn_merge(17, 4, 2, 64, parts, lses, 0x5000, 0x6000, None) == 2    # n > 16
+    assert L.ls_attn_merge(2, 4, 2, 60, parts, lses, 0x5000, 0x6000, None) == 2     # D % 8
+    assert L.ls_attn_merge(2, 4, 2, 64, None, lses, 0x5000, 0x6000, None) == 1
+    bad = (ctypes.c_void_p * 2)(0x1008, 0x2000)
+    assert L.ls_attn_merge(2, 4, 2, 64, bad, lses, 0x5000, 0x6000, None) == 4       # misaligned
+    assert L.ls_sum_bf16(2, 12, parts, 0x5000, None) == 2                           # count % 8
+    assert L.ls_sum_bf16(2, 16, None, 0x5000, None) == 1
     assert L.ls_replay_bwd_workspace_bytes(None, 4) == 0
     assert L.ls_prefix_destroy(None) == 0
 
