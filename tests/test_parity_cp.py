@@ -109,3 +109,40 @@ def test_merge_arguments_are_checked_before_launch():
         ls.attn_merge(parts, lses)               # more than 16 parts
     with pytest.raises(ls.LongStrawError):
         ls.sum_bf16([torch.zeros(12, dtype=torch.bfloat16, device="cuda")] * 2)   # count % 8
+
+
+def test_rank_driver_with_a_one_rank_group():
+    """long_context_grpo_gb300.cp.replay_response through a real (one-rank, NCCL) process
+    group on this GPU: the exchange is the identity, the results are the oracle's."""
+    import os
+    import socket
+    import torch.distributed as dist
+    from long_context_grpo_gb300 import cp
+    import long_context_grpo_gb300 as ls
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("nccl", rank=0, world_size=1)
+    try:
+        w = wl.small("rank_driver", 300, (130,), 8, 2, 128)
+        R, kp, vp, resp = make_group(w, seed=8)
+        dk = torch.empty(kp.shape, dtype=torch.float32, device="cuda")
+        dv = torch.empty_like(dk)
+        pre = ls.Prefix(kp, vp, dk, dv, Hq=w.Hq)
+        q, ks, vs, do = resp[0]
+        o, lse, dq, dks, dvs = cp.replay_response(pre, 0, 1, q, ks, vs, do)
+        dkf = torch.empty_like(dk)
+        dvf = torch.empty_like(dk)
+        pre.finalize(1.0, dkf, dvf, out_fp32=True)
+        torch.cuda.synchronize()
+        pre.close()
+    finally:
+        dist.destroy_process_group()
+    ref = oracle.replay_response(kp, vp, q, ks, vs, do)
+    assert rel_l2(o, ref["o"]) < TOL_BF16 and rel_l2(dq, ref["dq"]) < TOL_BF16
+    assert np.max(np.abs(f64(lse) - ref["lse"])) < TOL_LSE
+    assert rel_l2(dks, ref["dk_suffix"]) < TOL_BF16 and rel_l2(dvs, ref["dv_suffix"]) < TOL_BF16
+    assert rel_l2(dkf, ref["dk_prefix"]) < TOL_PREFIX and rel_l2(dvf, ref["dv_prefix"]) < TOL_PREFIX
