@@ -30,6 +30,11 @@
 // Warp roles (384 threads, one CTA per SM): warp 0 TMA producer, warp 1 one MMA-issuing
 // thread, warp 2 TMEM owner, warps 4-11 two softmax warpgroups; warpgroup w owns tile
 // columns [64 w, 64 w + 64).  Every wait is bounded (status word + clean exit on timeout).
+//
+// Instantiations <D, kPacked, kNoSuffix> as in the forward: packed responses (a prompt tile
+// then sweeps the Q tiles of every response before its single read-modify-write; Q rows past
+// a response's end carry +inf row statistics), or prompt keys only (context-parallel
+// shards).
 #include "ls_internal.h"
 #include "ptx.cuh"
 

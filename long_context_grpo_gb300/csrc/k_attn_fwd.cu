@@ -18,6 +18,10 @@
 // consecutive queries x the g query heads that share the kv head, so one K/V tile feeds
 // 2 x 128 rows of MMA.  Units are ordered kv-head-major so the CTAs running at the same
 // time stream the same prompt K/V through L2.
+// Instantiations: <D, kPacked, kNoSuffix>.  kPacked: several responses packed along the
+// token axis (units, Q rows and suffix keys offset by the response's packed row; each
+// response sees the prompt and only its own causal suffix).  kNoSuffix: prompt keys only
+// (one shard of a context-parallel prompt).  <D, false, false> is the one-response replay.
 // Every wait is bounded; on a timeout the CTA records it in the status word, drains its
 // in-flight copies and MMAs, frees TMEM and exits.
 #include "ls_internal.h"
