@@ -391,21 +391,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait();
           tc_fence_before();
           mbar_arrive(&bars[C::kBarSFree]);
+          // exponent arguments s c2 - LSE on fp32 pairs (one instruction per two queries)
+          const uint64_t c2x2 = f2_pack(c2, c2);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const float4 l4 = __ldg(lse4 + i);
-            p[4 * i + 0] = ex2_approx(fmaf(__uint_as_float(sa[4 * i + 0]), c2, -l4.x));
-            p[4 * i + 1] = ex2_approx(fmaf(__uint_as_float(sa[4 * i + 1]), c2, -l4.y));
-            p[4 * i + 2] = ex2_approx(fmaf(__uint_as_float(sa[4 * i + 2]), c2, -l4.z));
-            p[4 * i + 3] = ex2_approx(fmaf(__uint_as_float(sa[4 * i + 3]), c2, -l4.w));
+            float x0, x1, x2, x3;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sa[4 * i + 0]), __uint_as_float(sa[4 * i + 1])),
+                             c2x2, f2_pack(-l4.x, -l4.y)), x0, x1);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sa[4 * i + 2]), __uint_as_float(sa[4 * i + 3])),
+                             c2x2, f2_pack(-l4.z, -l4.w)), x2, x3);
+            p[4 * i + 0] = ex2_approx(x0);
+            p[4 * i + 1] = ex2_approx(x1);
+            p[4 * i + 2] = ex2_approx(x2);
+            p[4 * i + 3] = ex2_approx(x3);
           }
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const float4 l4 = __ldg(lse4 + 8 + i);
-            p[32 + 4 * i + 0] = ex2_approx(fmaf(__uint_as_float(sb[4 * i + 0]), c2, -l4.x));
-            p[32 + 4 * i + 1] = ex2_approx(fmaf(__uint_as_float(sb[4 * i + 1]), c2, -l4.y));
-            p[32 + 4 * i + 2] = ex2_approx(fmaf(__uint_as_float(sb[4 * i + 2]), c2, -l4.z));
-            p[32 + 4 * i + 3] = ex2_approx(fmaf(__uint_as_float(sb[4 * i + 3]), c2, -l4.w));
+            float x0, x1, x2, x3;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sb[4 * i + 0]), __uint_as_float(sb[4 * i + 1])),
+                             c2x2, f2_pack(-l4.x, -l4.y)), x0, x1);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sb[4 * i + 2]), __uint_as_float(sb[4 * i + 3])),
+                             c2x2, f2_pack(-l4.z, -l4.w)), x2, x3);
+            p[32 + 4 * i + 0] = ex2_approx(x0);
+            p[32 + 4 * i + 1] = ex2_approx(x1);
+            p[32 + 4 * i + 2] = ex2_approx(x2);
+            p[32 + 4 * i + 3] = ex2_approx(x3);
           }
         }
         // causal suffix: rows r < lo of the tile see only suffix keys < this key
@@ -434,10 +446,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 8; ++i) {
             const float4 d4 = __ldg(dlt4 + ch * 8 + i);
             const int c = ch * 32 + 4 * i;
-            const float s0 = p[c + 0] * (__uint_as_float(dv[4 * i + 0]) - d4.x);
-            const float s1 = p[c + 1] * (__uint_as_float(dv[4 * i + 1]) - d4.y);
-            const float s2 = p[c + 2] * (__uint_as_float(dv[4 * i + 2]) - d4.z);
-            const float s3 = p[c + 3] * (__uint_as_float(dv[4 * i + 3]) - d4.w);
+            // dS = P (dP - Delta) on fp32 pairs
+            float s0, s1, s2, s3;
+            f2_unpack(f2_mul(f2_pack(p[c + 0], p[c + 1]),
+                             f2_sub(f2_pack(__uint_as_float(dv[4 * i + 0]), __uint_as_float(dv[4 * i + 1])),
+                                    f2_pack(d4.x, d4.y))), s0, s1);
+            f2_unpack(f2_mul(f2_pack(p[c + 2], p[c + 3]),
+                             f2_sub(f2_pack(__uint_as_float(dv[4 * i + 2]), __uint_as_float(dv[4 * i + 3])),
+                                    f2_pack(d4.z, d4.w))), s2, s3);
             pw[2 * i] = pack_bf16x2(p[c + 0], p[c + 1]);
             pw[2 * i + 1] = pack_bf16x2(p[c + 2], p[c + 3]);
             dw[2 * i] = pack_bf16x2(s0, s1);
@@ -854,10 +870,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait();
           tc_fence_before();
           mbar_arrive(&bars[C::kBarSFree]);
+          // exponent arguments s c2 - LSE on fp32 pairs (one instruction per two keys)
+          const uint64_t c2x2 = f2_pack(c2, c2), nl2 = f2_pack(-lse2, -lse2);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            p[i] = ex2_approx(fmaf(__uint_as_float(sa[i]), c2, -lse2));
-            p[32 + i] = ex2_approx(fmaf(__uint_as_float(sb[i]), c2, -lse2));
+          for (int i = 0; i < 16; ++i) {
+            float x0, x1, y0, y1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sa[2 * i]), __uint_as_float(sa[2 * i + 1])),
+                             c2x2, nl2), x0, x1);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sb[2 * i]), __uint_as_float(sb[2 * i + 1])),
+                             c2x2, nl2), y0, y1);
+            p[2 * i] = ex2_approx(x0);
+            p[2 * i + 1] = ex2_approx(x1);
+            p[32 + 2 * i] = ex2_approx(y0);
+            p[32 + 2 * i + 1] = ex2_approx(y1);
           }
         }
         if (lim < wg * 64 + 64) {
@@ -877,10 +902,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(lane_base + col, dv);
           tmem_ld_wait();
           uint32_t dw[16];
+          const uint64_t dlt2 = f2_pack(dlt, dlt);
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            dw[i] = pack_bf16x2(p[ch * 32 + 2 * i] * (__uint_as_float(dv[2 * i]) - dlt),
-                                p[ch * 32 + 2 * i + 1] * (__uint_as_float(dv[2 * i + 1]) - dlt));
+          for (int i = 0; i < 16; ++i) {
+            // dS = P (dP - Delta) on fp32 pairs
+            float s0, s1;
+            f2_unpack(f2_mul(f2_pack(p[ch * 32 + 2 * i], p[ch * 32 + 2 * i + 1]),
+                             f2_sub(f2_pack(__uint_as_float(dv[2 * i]), __uint_as_float(dv[2 * i + 1])),
+                                    dlt2)), s0, s1);
+            dw[i] = pack_bf16x2(s0, s1);
+          }
           tmem_st16(lane_base + col, dw);
         }
         tmem_st_wait();

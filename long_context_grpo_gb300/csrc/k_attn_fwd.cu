@@ -393,22 +393,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           resc = true;
         }
         const float neg_m = (m_run == -INFINITY) ? 0.0f : -m_run;
-        float rs = 0.0f;
+        // exponent arguments and the row sum on fp32 pairs (one instruction per two keys)
+        const uint64_t c2x2 = f2_pack(c2, c2), nm2 = f2_pack(neg_m, neg_m);
+        uint64_t rs2 = f2_pack(0.0f, 0.0f);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t pw[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int c = half * 64 + 2 * i;
-            const float p0 = ex2_approx(fmaf(__uint_as_float(sv[c >> 5][c & 31]), c2, neg_m));
-            const float p1 =
-                ex2_approx(fmaf(__uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]), c2, neg_m));
-            rs += p0 + p1;
+            const uint64_t a = f2_fma(f2_pack(__uint_as_float(sv[c >> 5][c & 31]),
+                                              __uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31])),
+                                      c2x2, nm2);
+            float x0, x1;
+            f2_unpack(a, x0, x1);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            rs2 = f2_add(rs2, f2_pack(p0, p1));
             pw[i] = pack_bf16x2(p0, p1);
           }
           tmem_st32(lane_base + colS + half * 32, pw);
         }
-        l += rs;
+        float rs0, rs1;
+        f2_unpack(rs2, rs0, rs1);
+        l += rs0 + rs1;
         if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll
           for (int cc = 0; cc < D / 32; ++cc) {
