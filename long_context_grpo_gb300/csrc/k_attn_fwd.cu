@@ -380,7 +380,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (c >= lim) sv[c >> 5][c & 31] = __float_as_uint(-INFINITY);
         }
 #pragma unroll
-        for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sv[c >> 5][c & 31]));
+        for (int c = 0; c < 128; c += 2)
+          mx = fmax3(mx, __uint_as_float(sv[c >> 5][c & 31]), __uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]));
         const float mt = mx * c2;
         float factor = 1.0f;
         bool resc = false;

@@ -404,6 +404,13 @@ __device__ __forceinline__ void tmem_st_wait() {
 // ---------------------------------------------------------------------------------------
 // Small numeric helpers
 // ---------------------------------------------------------------------------------------
+// Maximum of three fp32 values in one instruction (sm_100+); exact, like fmaxf twice.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // Packed fp32 pairs (two independent round-to-nearest lanes per instruction; sm_100+).
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
   uint64_t r;
