@@ -1,0 +1,59 @@
+"""The measurement code on the CPU: the algorithmic work formula, the traffic record's
+source gating, and the reference arm's JSON line (every key the benchmark contract asks
+for)."""
+import json
+import os
+
+import pytest
+
+import bench
+
+
+def test_pairs_counts_visible_query_key_pairs():
+    # brute force: suffix row t sees every prompt key and suffix keys 0..t
+    for P in (0, 1, 5, 17):
+        for R in (1, 2, 9):
+            n = sum(1 for t in range(R) for j in range(P + R) if j < P or j - P <= t)
+            assert bench.pairs(P, R) == n
+
+
+def test_traffic_is_scaled_by_work_units_and_gated_by_the_source_hash(tmp_path, monkeypatch):
+    from long_context_grpo_gb300 import workloads as wl
+    w = wl.WORKLOADS["p2m"]
+    t = bench.load_traffic(w, [128, 256])
+    rec = json.load(open(os.path.join(bench.ROOT, "profiles", "ncu_traffic.json")))["bwd_dkdv"]
+    units = [w.Hkv * (w.P // 128 + 1), w.Hkv * (w.P // 128 + 2)]
+    assert t == pytest.approx(rec["dram_bytes_per_unit"] * sum(units) / 2)
+    # a record whose hash no longer matches the kernel source gives no number
+    fake = dict(rec, kernel_source_sha256_16="0" * 16)
+    os.makedirs(tmp_path / "profiles")
+    json.dump({"bwd_dkdv": fake}, open(tmp_path / "profiles" / "ncu_traffic.json", "w"))
+    src = tmp_path / rec["kernel_source"]
+    os.makedirs(src.parent, exist_ok=True)
+    src.write_bytes(open(os.path.join(bench.ROOT, rec["kernel_source"]), "rb").read())
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.load_traffic(w, [128]) is None
+
+
+def test_reference_arm_prints_one_complete_json_line(monkeypatch, capsys):
+    monkeypatch.delenv("RANK", raising=False)
+    monkeypatch.setattr("sys.argv", ["bench.py", "--impl", "reference", "--workload", "tiny",
+                                     "--steps", "1", "--warmup", "3", "--cpu-rows", "2"])
+    bench.main()
+    out = capsys.readouterr().out.strip().splitlines()
+    assert len(out) == 1
+    d = json.loads(out[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "impl", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["value"] > 0 and d["steps"] == 1
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["config"]["workload"] == "tiny"
+
+
+def test_warmup_below_three_is_refused(monkeypatch):
+    monkeypatch.setattr("sys.argv", ["bench.py", "--warmup", "2"])
+    with pytest.raises(SystemExit):
+        bench.main()
