@@ -962,12 +962,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, bool kPacked, bool kNoSuffix = false>
 cudaError_t launch_dkdv_d(const BwdArgs& a, cudaStream_t s) {
   using C = DkdvCfg<D>;
-  static bool attr_set = false;
-  if (!attr_set) {
+  // the shared-memory opt-in is per device: remember it per device index
+  static bool attr_set[kMaxDeviceCache] = {};
+  const int dev = cached_device_index();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D, kPacked, kNoSuffix>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set[dev] = true;
   }
   const int64_t n_units =
       static_cast<int64_t>(a.sh.Hkv) * ((a.sh.P + 127) / 128 + (kNoSuffix ? 0 : a.vl.kt0[a.vl.G]));
@@ -982,12 +985,15 @@ cudaError_t launch_dkdv_d(const BwdArgs& a, cudaStream_t s) {
 template <int D, bool kPacked, bool kNoSuffix = false>
 cudaError_t launch_dq_d(const BwdArgs& a, cudaStream_t s) {
   using C = DqCfg<D>;
-  static bool attr_set = false;
-  if (!attr_set) {
+  // the shared-memory opt-in is per device: remember it per device index
+  static bool attr_set[kMaxDeviceCache] = {};
+  const int dev = cached_device_index();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(attn_bwd_dq_kernel<D, kPacked, kNoSuffix>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set[dev] = true;
   }
   const int64_t n_units = static_cast<int64_t>(a.sh.Hkv) * a.vl.qt0[a.vl.G];
   int grid = num_sms();

@@ -480,12 +480,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, bool kPacked, bool kNoSuffix = false>
 cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t s) {
   using C = FwdCfg<D>;
-  static bool attr_set = false;
-  if (!attr_set) {
+  // the shared-memory opt-in is per device: remember it per device index
+  static bool attr_set[kMaxDeviceCache] = {};
+  const int dev = cached_device_index();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, kPacked, kNoSuffix>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set[dev] = true;
   }
   const int64_t n_units = static_cast<int64_t>(a.sh.Hkv) * a.vl.pair0[a.vl.G];
   int grid = num_sms();

@@ -144,6 +144,13 @@ cudaError_t launch_attn_bwd_dkdv(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_attn_bwd_dq(const BwdArgs& a, cudaStream_t s);
 
 int num_sms();
+// Current device index for per-device host caches (launch attributes); -1 if unusable.
+constexpr int kMaxDeviceCache = 64;
+inline int cached_device_index() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDeviceCache) return -1;
+  return dev;
+}
 // Status word of the current device (returns an ls_status value) and the per-thread
 // message behind ls_last_error(); both live in ls_api.cu.
 int device_status_word(uint32_t** out);
