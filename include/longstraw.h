@@ -17,8 +17,9 @@
  * Around that sequence: ls_token_logp (+ ls_replay_fwd) scores responses without
  * gradients (old/reference policy); ls_block_replay_fwd/bwd replay one long response block
  * by block (section 3-2 (4)); ls_replay_fwd_packed/bwd_packed replay a whole group in one
- * launch per kernel; a handle may be kept across groups (prefix reuse, section 4-2) with
- * ls_prefix_grad_finalize(..., reset_acc = 1) between them.
+ * launch per kernel; ls_replay_*_prompt_only with ls_attn_merge and ls_sum_bf16 split the
+ * prompt into context-parallel shards (section 3-2 (2)); a handle may be kept across groups
+ * (prefix reuse, section 4-2) with ls_prefix_grad_finalize(..., reset_acc = 1) between them.
  *
  * Conventions shared by every entry point
  *  - Pointers named "device" must point to device memory of the current CUDA device,
