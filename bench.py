@@ -75,13 +75,44 @@ def rank_sum(x, dist=None, device="cpu"):
 
 
 def load_peaks():
+    """The measured peaks (copy bandwidth, cuBLAS bf16 burst and sustained) and the
+    median SM clock under load while they were measured (None if not recorded)."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+        peaks = {k: float(d[k]) for k in FALLBACK_PEAKS}
+        peaks["sm_mhz"] = (d.get("clocks_under_load") or {}).get("sm_mhz_median")
+        return peaks, "measured"
     except Exception:
-        return dict(FALLBACK_PEAKS), "fallback"
+        out = dict(FALLBACK_PEAKS)
+        out["sm_mhz"] = None
+        return out, "fallback"
+
+
+# Dense bf16 tensor figures of the GPU, for context beside the measured peaks: NVIDIA's
+# nominal dense bf16 rate, and the tensor pipe's issue rate (8192 bf16 FLOP per clock per SM
+# for the 128 x N x 16 instruction shapes used here) at the clock a run actually held.
+NOMINAL_DENSE_BF16_TFLOPS = 2250.0
+TENSOR_FLOP_PER_CLK_PER_SM = 8192
+
+
+def tensor_context(achieved, peaks, run_mhz, n_sms):
+    """Fractions of a contraction's achieved TFLOP/s against other denominators than the
+    contract's sustained cuBLAS figure: the cuBLAS burst figure, the nominal dense rate, the
+    tensor pipe at the run's median clock, and the sustained figure rescaled to the run's
+    clock (the peak was measured under the power cap at a lower clock)."""
+    out = {"frac_of_burst": achieved / peaks["bf16_tflops"],
+           "frac_of_nominal_dense": achieved / NOMINAL_DENSE_BF16_TFLOPS,
+           "run_sm_mhz": run_mhz, "peak_sm_mhz": peaks.get("sm_mhz")}
+    if run_mhz:
+        pipe = TENSOR_FLOP_PER_CLK_PER_SM * n_sms * run_mhz * 1e6 / 1e12
+        out["tensor_pipe_tflops_at_run_clock"] = pipe
+        out["frac_of_tensor_pipe_at_run_clock"] = achieved / pipe
+        if peaks.get("sm_mhz"):
+            out["frac_of_sustained_per_clock"] = (achieved / run_mhz) / (
+                peaks["bf16_tflops_sustained"] / peaks["sm_mhz"])
+    return out
 
 
 # ------------------------------------------------------------------------------ clocks
@@ -263,10 +294,12 @@ class Group:
             out.append([r["q"], r["ks"], r["vs"], r["do"], r["logits"], r["ids"], r["old"]])
         return out
 
-    def step(self, loss_slot, ev_in=None, ev_used=None):
+    def step(self, loss_slot, ev_in=None, ev_used=None, out=None):
         """One group step.  With events (end-to-end runs): input group k is waited for
         (ev_in[k]) before its first use and ev_used[k] is recorded after its last use, so
-        the copies of later responses overlap the replay of earlier ones."""
+        the copies of later responses overlap the replay of earlier ones.  With `out` (a
+        HostResults), each response's results and the finalized prompt gradient are copied
+        back to the host as soon as they are written, overlapping the rest of the step."""
         import torch
         import long_context_grpo_gb300 as ls
         w = self.w
@@ -278,6 +311,8 @@ class Group:
             if ev_in is not None:
                 cur.wait_event(ev_in[1 + i])
             o, lse = pre.fwd(r["q"], r["ks"], r["vs"], o=self.o[:Ri], lse=self.lse[:Ri])
+            if out is not None:
+                out.before_response(cur)
             ls.grpo_loss(r["logits"], r["ids"], r["old"], self.A[i], w.eps, w.G, loss_slot,
                          dlogits=self.dlog[:Ri], clip_mask=self.mask[:Ri],
                          logp_out=self.logp[:Ri], workspace=self.lws)
@@ -285,9 +320,15 @@ class Group:
                     dk_suffix=self.dks[:Ri], dv_suffix=self.dvs[:Ri], workspace=self.bws)
             if ev_used is not None:
                 ev_used[1 + i].record(cur)
+            if out is not None:
+                out.response_done(i, cur)
         if ev_used is not None:
             ev_used[0].record(cur)
+        if out is not None:
+            out.before_finalize(cur)
         pre.finalize(1.0, self.dk_out, self.dv_out)
+        if out is not None:
+            out.finalize_done(cur)
         pre.close()
 
     def score(self):
@@ -485,6 +526,138 @@ class Group:
         }
 
 
+class HostResults:
+    """Pinned host copies of one step's results, filled on a copy stream while the step
+    runs: per response dQ, suffix dK/dV, clip mask and token log-prob (as soon as that
+    response's backward has written them), and the finalized prompt dK/dV at the end.  The
+    compute stream reuses the device buffers only after the previous copy out of them has
+    completed.  dlogits stay on the device (they feed the LM-head backward there)."""
+
+    def __init__(self, grp, copy_stream):
+        import torch
+        self.grp, self.cs = grp, copy_stream
+        w = grp.w
+
+        def pin(shape, dtype):
+            return torch.empty(shape, dtype=dtype, pin_memory=True)
+
+        self.resp = [{"dq": pin((Ri, w.Hq, w.D), torch.bfloat16),
+                      "dks": pin((Ri, w.Hkv, w.D), torch.bfloat16),
+                      "dvs": pin((Ri, w.Hkv, w.D), torch.bfloat16),
+                      "mask": pin((Ri,), torch.uint8), "logp": pin((Ri,), torch.float32)}
+                     for Ri in grp.R]
+        self.dk = pin(tuple(grp.dk_out.shape), torch.bfloat16)
+        self.dv = pin(tuple(grp.dv_out.shape), torch.bfloat16)
+        self.bytes = sum(t.numel() * t.element_size() for d in self.resp for t in d.values())
+        self.bytes += 2 * self.dk.numel() * self.dk.element_size()
+        self.resp_copied = None     # copy of the last response's outputs finished
+        self.fin_copied = None      # copy of the finalized prompt gradient finished
+
+    def before_response(self, cur):
+        if self.resp_copied is not None:
+            cur.wait_event(self.resp_copied)
+
+    def response_done(self, i, cur):
+        import torch
+        g, Ri = self.grp, self.grp.R[i]
+        ready = torch.cuda.Event()
+        ready.record(cur)
+        self.cs.wait_event(ready)
+        h = self.resp[i]
+        with torch.cuda.stream(self.cs):
+            h["dq"].copy_(g.dq[:Ri], non_blocking=True)
+            h["dks"].copy_(g.dks[:Ri], non_blocking=True)
+            h["dvs"].copy_(g.dvs[:Ri], non_blocking=True)
+            h["mask"].copy_(g.mask[:Ri], non_blocking=True)
+            h["logp"].copy_(g.logp[:Ri], non_blocking=True)
+        self.resp_copied = torch.cuda.Event()
+        self.resp_copied.record(self.cs)
+
+    def before_finalize(self, cur):
+        if self.fin_copied is not None:
+            cur.wait_event(self.fin_copied)
+
+    def finalize_done(self, cur):
+        import torch
+        ready = torch.cuda.Event()
+        ready.record(cur)
+        self.cs.wait_event(ready)
+        with torch.cuda.stream(self.cs):
+            self.dk.copy_(self.grp.dk_out, non_blocking=True)
+            self.dv.copy_(self.grp.dv_out, non_blocking=True)
+        self.fin_copied = torch.cuda.Event()
+        self.fin_copied.record(self.cs)
+
+
+def time_group(grp, steps, warmup, stream, peaks, n_sms, losses):
+    """Warm-up and timed steps of one group on this GPU (CUDA events on `stream`, every
+    library launch timed on its own stream): (ms per step, per-kernel table)."""
+    import torch
+    import long_context_grpo_gb300 as ls
+    for k in range(warmup):
+        grp.step(losses[k % losses.numel():k % losses.numel() + 1])
+    torch.cuda.synchronize()
+    ls.timing_read()
+    ls.timing_enable(True)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(steps):
+        grp.step(losses[k % losses.numel():k % losses.numel() + 1])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ls.timing_enable(False)
+    kt = ls.timing_read()
+    ms = e0.elapsed_time(e1)
+    return ms / steps, kernel_table(kt, grp.kernel_work(), steps, ms, peaks)
+
+
+def kernel_table(kt, work, steps, total_ms, peaks):
+    """Per kernel: launches, average ms, share of the timed region, achieved rate against
+    the measured peak of its bound (sustained bf16 for contractions, HBM copy otherwise)."""
+    kernels = {}
+    for name, (tot_ms, n) in kt.items():
+        if n == 0 or tot_ms <= 0:
+            continue
+        amount, unit = work[name]
+        per_launch_amount = amount * steps / n
+        avg_ms = tot_ms / n
+        if unit == "flop":
+            ach = per_launch_amount / (avg_ms / 1e3) / 1e12
+            pk, pu, bound = peaks["bf16_tflops_sustained"], "TFLOP/s", "tensor"
+        else:
+            ach = per_launch_amount / (avg_ms / 1e3) / 1e9
+            pk, pu, bound = peaks["hbm_gbs"], "GB/s", "hbm"
+        kernels[name] = {"launches": n, "avg_ms": avg_ms, "share": tot_ms / total_ms,
+                         "bound": bound, "achieved": ach, "peak": pk, "unit": pu,
+                         "frac": ach / pk}
+    return kernels
+
+
+def measure_configs(names, args, dev, stream, peaks, n_sms):
+    """Throughput of the whole group step on the other workload configurations (the same
+    step, launch configuration and timing as the headline measurement), one at a time."""
+    import torch
+    from long_context_grpo_gb300 import workloads as wl
+    out = {}
+    losses = torch.zeros(4, dtype=torch.float64, device=dev)
+    for name in names:
+        w = wl.WORKLOADS[name]
+        grp = Group(w, args.seed, dev)
+        ms, kernels = time_group(grp, args.config_steps, args.warmup, stream, peaks, n_sms,
+                                 losses)
+        out[name] = {"value": grp.flops() / (ms / 1e3) / 1e12, "unit": "TFLOP/s",
+                     "response_tok_s": sum(grp.R) / (ms / 1e3), "ms_per_step": ms,
+                     "steps": args.config_steps, "P": w.P, "G": w.G, "R": grp.R,
+                     "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D, "V": w.V,
+                     "kernels": {k: {"frac": round(v["frac"], 4), "achieved": round(v["achieved"], 1),
+                                     "unit": v["unit"], "share": round(v["share"], 4)}
+                                 for k, v in kernels.items()}}
+        del grp
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, w):
     import torch
     import long_context_grpo_gb300 as ls
@@ -554,29 +727,23 @@ def run_ours(args, w):
 
     # ---------------- per-kernel roofline
     peaks, peak_src = load_peaks()
-    work = grp.kernel_work()
-    kernels = {}
-    for name, (tot_ms, n) in kt.items():
-        if n == 0 or tot_ms <= 0:
-            continue
-        amount, unit = work[name]
-        per_launch_amount = amount * args.steps / n
-        avg_ms = tot_ms / n
-        if unit == "flop":
-            ach = per_launch_amount / (avg_ms / 1e3) / 1e12
-            pk, pu, bound = peaks["bf16_tflops_sustained"], "TFLOP/s", "tensor"
-        else:
-            ach = per_launch_amount / (avg_ms / 1e3) / 1e9
-            pk, pu, bound = peaks["hbm_gbs"], "GB/s", "hbm"
-        kernels[name] = {"launches": n, "avg_ms": avg_ms, "share": tot_ms / ms,
-                         "bound": bound, "achieved": ach, "peak": pk, "unit": pu,
-                         "frac": ach / pk}
+    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    kernels = kernel_table(kt, grp.kernel_work(), args.steps, ms, peaks)
+    for name, kd in kernels.items():
+        if kd["bound"] == "tensor":
+            kd.update(tensor_context(kd["achieved"], peaks, clk.get("sm_mhz"), n_sms))
     dom = max(kernels, key=lambda k: kernels[k]["share"])
     d = kernels[dom]
     traffic = load_traffic(w, grp.R) if dom == "bwd_dkdv" else None
     roofline = {"kernel": dom, "bound": d["bound"], "achieved": d["achieved"], "peak": d["peak"],
                 "unit": d["unit"], "frac": d["frac"], "traffic": traffic,
                 "peak_source": peak_src + (" sustained bf16" if d["bound"] == "tensor" else " HBM copy")}
+    if d["bound"] == "tensor":
+        roofline.update({k: d[k] for k in d if k.startswith("frac_of") or k.endswith("mhz")
+                         or k.startswith("tensor_pipe")})
+    # the whole step (all kernels, algorithmic FLOPs) against the same denominators
+    step_context = tensor_context(value, peaks, clk.get("sm_mhz"), n_sms)
+    step_context["frac_of_sustained"] = value / peaks["bf16_tflops_sustained"]
     launches = sum(v["launches"] * KERNELS_PER_BRACKET.get(k, 1) for k, v in kernels.items())
 
     # ---------------- old/reference-policy scoring of the same group (no gradients)
@@ -637,7 +804,9 @@ def run_ours(args, w):
             host_groups.append(hg)
         h2d = sum(t.numel() * t.element_size() for hg in host_groups for t in hg)
         host_loss = torch.empty(1, dtype=torch.float64).pin_memory()
-        copy_stream = torch.cuda.Stream()
+        copy_stream = torch.cuda.Stream()      # host -> device, in consumption order
+        back_stream = torch.cuda.Stream()      # device -> host, as results are written
+        results = HostResults(grp, back_stream)
         ev_in = [torch.cuda.Event() for _ in dev_groups]
         ev_used = [torch.cuda.Event() for _ in dev_groups]
         steps_done = [0]
@@ -650,7 +819,7 @@ def run_ours(args, w):
                     for h, d_ in zip(hg, dg):
                         d_.copy_(h, non_blocking=True)
                 ev_in[k].record(copy_stream)
-            grp.step(losses[slot:slot + 1], ev_in=ev_in, ev_used=ev_used)
+            grp.step(losses[slot:slot + 1], ev_in=ev_in, ev_used=ev_used, out=results)
             host_loss.copy_(losses[slot:slot + 1], non_blocking=True)
             steps_done[0] += 1
 
@@ -663,8 +832,10 @@ def run_ours(args, w):
         ls.timing_enable(True)
         e0.record(stream)
         copy_stream.wait_event(e0)
+        back_stream.wait_event(e0)
         for _ in range(args.steps):
             e2e_step()
+        stream.wait_event(results.fin_copied)   # the last read-back is inside the timed region
         e1.record(stream)
         torch.cuda.synchronize()
         ls.timing_enable(False)
@@ -672,22 +843,36 @@ def run_ours(args, w):
         ems = max_over_ranks(e0.elapsed_time(e1))
         e2e = {"value": flops_all / (ems / 1e3) / 1e12, "unit": "TFLOP/s",
                "response_tok_s": toks_all / (ems / 1e3), "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": 8,
+               "d2h_bytes_per_step": results.bytes + 8,
+               "d2h": "per response dQ, suffix dK/dV, clip mask and token log-prob, the "
+                      "finalized bf16 prompt dK/dV and the fp64 loss; dlogits stay on the device",
                "kernel_ms_per_step": {k: round(v[0] / args.steps, 2) for k, v in e2e_k.items() if v[1] > 0}}
-        del host_groups
+        del host_groups, results
 
     # ---------------- CPU baseline (rank 0, N = 1 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        # timed as the reference arm times it: warm-up samples, then several timed samples
         rows = args.cpu_rows
         inp = cpu_sample_inputs(w, args.seed, rows)
+        for _ in range(args.cpu_warmup):
+            oracle_sample_step(w, inp, w.G)
         t0 = time.perf_counter()
-        fl = oracle_sample_step(w, inp, w.G)
+        fl = 0
+        for _ in range(args.cpu_steps):
+            fl += oracle_sample_step(w, inp, w.G)
         dt = time.perf_counter() - t0
         cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cores(), "kind": "oracle",
                "sample": "float64 oracle, %d query rows x 1 of %d query heads of response 0 "
                          "against the full %d-token prompt (fwd + bwd) plus their GRPO loss; "
-                         "%.1f s" % (rows, w.Hq, w.P, dt)}
+                         "%d warm-up + %d timed samples, %.1f s timed"
+                         % (rows, w.Hq, w.P, args.cpu_warmup, args.cpu_steps, dt)}
+
+    # ---------------- the other workload configurations (rank 0, whole group step each)
+    configs = None
+    names = [n for n in args.configs.split(",") if n and n != w.name]
+    if names and rank == 0:
+        configs = measure_configs(names, args, dev, stream, peaks, n_sms)
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -701,6 +886,7 @@ def run_ours(args, w):
                            "l2": "inputs larger than L2 (no flush)"},
                 "response_tok_s": tok_s,
                 "roofline": roofline,
+                "step_vs_peaks": step_context,
                 "kernels": kernels,
                 "gpu_launches": launches,
                 "clocks": clk,
@@ -710,6 +896,7 @@ def run_ours(args, w):
                 "block_replay": blk,
                 "packed_replay": packed,
                 "cp_replay": cp,
+                "other_configs": configs,
                 "receipt": {"gradient_semantics": "prompt dK/dV exposed (fp32, group-summed), "
                                                   "not propagated",
                             "residency": "prompt K/V resident in HBM for the group",
@@ -729,12 +916,17 @@ def main():
     ap.add_argument("--workload", default="p2m")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-rows", type=int, default=8)
+    ap.add_argument("--cpu-warmup", type=int, default=1)
+    ap.add_argument("--cpu-steps", type=int, default=3)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-score", action="store_true")
     ap.add_argument("--no-packed", action="store_true")
     ap.add_argument("--cp-shards", type=int, default=8,
                     help="prompt shards of the context-parallel measurement (0: skip it)")
+    ap.add_argument("--configs", default="tiny,p32k,p262k,p1m",
+                    help="other workloads whose group step is timed too ('' : none)")
+    ap.add_argument("--config-steps", type=int, default=2)
     ap.add_argument("--block", type=int, default=4096,
                     help="block length of the blockwise-replay measurement (0: skip it)")
     args = ap.parse_args()

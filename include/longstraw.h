@@ -224,6 +224,10 @@ size_t ls_grpo_loss_workspace_bytes(int64_t R);
  * are fp64; the clip decision and g use rho evaluated in fp32 from the fp64 log-ratio
  * (relative error ~2e-7, so the mask equals an exact evaluation except for rho within
  * ~1e-6 of 1 +- eps).  The loss reduction is a fixed-order tree (deterministic).
+ * Failure: if a bounded wait inside the kernel gives up (ls_get_device_status then returns
+ * LS_ERR_TIMEOUT), every row not finished before it gets a NaN loss term (so *loss_accum
+ * becomes NaN), a zero dlogits row, clip_mask 0 and a NaN logp_out; the call itself still
+ * returns LS_OK, since the failure happens after it returned.
  */
 ls_status ls_grpo_loss(int64_t R, int64_t V, int32_t G, const void* logits, const int32_t* ids,
                        const float* logp_old, double advantage, double eps, double* loss_accum,
@@ -238,7 +242,8 @@ ls_status ls_grpo_loss(int64_t R, int64_t V, int32_t G, const void* logits, cons
  *   logits device bf16 [R, V]; ids device int32 [R] (an id outside [0, V) sets the device
  *   status and gives 0); logp_out device fp32 [R] (written).  One read of the logits; the
  *   row log-sum-exp is combined in fp64 as in ls_grpo_loss (so the values are identical to
- *   ls_grpo_loss's logp_out).  The attention part of scoring is ls_replay_fwd.
+ *   ls_grpo_loss's logp_out).  The attention part of scoring is ls_replay_fwd.  Rows left
+ *   unfinished by a bounded wait that gave up (LS_ERR_TIMEOUT) get a NaN log-prob.
  */
 ls_status ls_token_logp(int64_t R, int64_t V, const void* logits, const int32_t* ids,
                         float* logp_out, void* stream);
@@ -259,8 +264,10 @@ ls_status ls_token_logp(int64_t R, int64_t V, const void* logits, const int32_t*
  *   that device current); make that first call before any stream capture.
  *   All calls on a device share the scratch: calls whose kernels may overlap on the GPU
  *   (unordered streams or threads) race; calls ordered on one stream are safe.  Every
- *   scratch entry a call reads was written earlier in the same call, so no clearing is
- *   needed between calls.
+ *   scratch entry a call reads was written earlier in the same call (a row left unfinished
+ *   by a bounded wait that gave up writes NaN, as in ls_grpo_loss), so no clearing is
+ *   needed between calls.  The stream must belong to the current device
+ *   (LS_ERR_WRONG_DEVICE otherwise), as for ls_grpo_loss.
  */
 ls_status ls_grpo_loss_noalloc(int64_t R, int64_t V, int32_t G, const void* logits,
                                const int32_t* ids, const float* logp_old, double advantage,

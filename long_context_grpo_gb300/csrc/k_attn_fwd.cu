@@ -373,15 +373,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int v = t - k0 + 1;
           lim = v < 0 ? 0 : (v > 128 ? 128 : v);
         }
-        float mx = -INFINITY;
         if (lim < 128) {
 #pragma unroll
           for (int c = 0; c < 128; ++c)
             if (c >= lim) sv[c >> 5][c & 31] = __float_as_uint(-INFINITY);
         }
+        // row maximum: four independent chains of three-input maxima (exact in any order),
+        // so the dependent chain is 16 deep instead of 64
+        float mxa = -INFINITY, mxb = -INFINITY, mxc = -INFINITY, mxd = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 128; c += 2)
-          mx = fmax3(mx, __uint_as_float(sv[c >> 5][c & 31]), __uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]));
+        for (int c = 0; c < 128; c += 8) {
+          mxa = fmax3(mxa, __uint_as_float(sv[c >> 5][c & 31]), __uint_as_float(sv[c >> 5][(c + 1) & 31]));
+          mxb = fmax3(mxb, __uint_as_float(sv[c >> 5][(c + 2) & 31]), __uint_as_float(sv[c >> 5][(c + 3) & 31]));
+          mxc = fmax3(mxc, __uint_as_float(sv[c >> 5][(c + 4) & 31]), __uint_as_float(sv[c >> 5][(c + 5) & 31]));
+          mxd = fmax3(mxd, __uint_as_float(sv[c >> 5][(c + 6) & 31]), __uint_as_float(sv[c >> 5][(c + 7) & 31]));
+        }
+        const float mx = fmax3(mxa, mxb, fmaxf(mxc, mxd));
         const float mt = mx * c2;
         float factor = 1.0f;
         bool resc = false;
@@ -394,9 +401,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           resc = true;
         }
         const float neg_m = (m_run == -INFINITY) ? 0.0f : -m_run;
-        // exponent arguments and the row sum on fp32 pairs (one instruction per two keys)
+        // exponent arguments and the row sum on fp32 pairs (one instruction per two keys);
+        // the sum runs in four independent pair accumulators (16-deep dependent chains)
         const uint64_t c2x2 = f2_pack(c2, c2), nm2 = f2_pack(neg_m, neg_m);
-        uint64_t rs2 = f2_pack(0.0f, 0.0f);
+        uint64_t rs2[4] = {f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f),
+                           f2_pack(0.0f, 0.0f)};
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t pw[32];
@@ -409,14 +418,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             float x0, x1;
             f2_unpack(a, x0, x1);
             const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-            rs2 = f2_add(rs2, f2_pack(p0, p1));
+            rs2[i & 3] = f2_add(rs2[i & 3], f2_pack(p0, p1));
             pw[i] = pack_bf16x2(p0, p1);
           }
           tmem_st32(lane_base + colS + half * 32, pw);
         }
-        float rs0, rs1;
-        f2_unpack(rs2, rs0, rs1);
-        l += rs0 + rs1;
+        float rs0, rs1, rs2f, rs3;
+        f2_unpack(f2_add(rs2[0], rs2[1]), rs0, rs1);
+        f2_unpack(f2_add(rs2[2], rs2[3]), rs2f, rs3);
+        l += (rs0 + rs1) + (rs2f + rs3);
         if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll
           for (int cc = 0; cc < D / 32; ++cc) {

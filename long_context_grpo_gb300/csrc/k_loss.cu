@@ -343,6 +343,10 @@ __global__ void __launch_bounds__(kClThreads, 4) grpo_loss_cluster(LossArgs a, i
   __shared__ float slot[2][kCl][3];              // per rank, row parity
   __shared__ float sh_g[2], sh_lse2[2];
   __shared__ int sh_yl[2];
+  // Set to 1 when a bounded wait of this CTA or of a peer gave up: from then on no CTA of
+  // the cluster exchanges partials any more, rows are only walked through (same barrier
+  // sequence, no loads) and their loss terms and log-probs are written as NaN.
+  __shared__ int cl_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_ctarank();
@@ -353,6 +357,7 @@ __global__ void __launch_bounds__(kClThreads, 4) grpo_loss_cluster(LossArgs a, i
   const int nvec = static_cast<int>(clen >> 3);
 
   if (tid == 0) {
+    cl_abort = 0;
     mbar_init(&xbar[0], kCl);
     mbar_init(&xbar[1], kCl);
     fence_mbar_init();
@@ -361,6 +366,7 @@ __global__ void __launch_bounds__(kClThreads, 4) grpo_loss_cluster(LossArgs a, i
   cluster_sync_all();   // peers' barriers are initialised before any remote arrive
 
   const int64_t cid = cluster_id_x(), ncl = cluster_count_x();
+  volatile int* vabort = &cl_abort;
 
   if (warp == kCWarps) {
     // ------------------------------------------------------------------ scalar warp
@@ -391,20 +397,57 @@ __global__ void __launch_bounds__(kClThreads, 4) grpo_loss_cluster(LossArgs a, i
         ms_merge(m, h, l, m2, h2, l2);
       }
       // lane 0: exchange, lse, and (loss) the clip decision and g
-      bool bad = false, clipped = false;
+      bool bad = false, clipped = false, aborted = false;
       double logp = 0.0, dl = 0.0;
       if (lane == 0) {
+        aborted = *vabort != 0;
+        if (!aborted) {
 #pragma unroll
-        for (int r = 0; r < kCl; ++r) {
-          const uint32_t dst = cluster_map(&slot[par][rank][0], r);
-          st_cluster_f32(dst, m);
-          st_cluster_f32(dst + 4, h);
-          st_cluster_f32(dst + 8, l);
+          for (int r = 0; r < kCl; ++r) {
+            const uint32_t dst = cluster_map(&slot[par][rank][0], r);
+            st_cluster_f32(dst, m);
+            st_cluster_f32(dst + 4, h);
+            st_cluster_f32(dst + 8, l);
+          }
+          // xbar[par] completes one phase every second row
+#pragma unroll
+          for (int r = 0; r < kCl; ++r) mbar_arrive_remote(cluster_map(&xbar[par], r));
+          aborted = !mbar_wait_cluster(&xbar[par], static_cast<uint32_t>((it >> 1) & 1), a.status,
+                                       vabort);
+          // a wait that gave up stops the exchange in every CTA of the cluster (the peers'
+          // own waits poll the flag); the CTAs stay resident until the final cluster barrier
+          if (aborted) {
+#pragma unroll
+            for (int r = 0; r < kCl; ++r) st_cluster_u32(cluster_map(&cl_abort, r), 1u);
+          }
         }
-        // xbar[par] completes one phase every second row
-#pragma unroll
-        for (int r = 0; r < kCl; ++r) mbar_arrive_remote(cluster_map(&xbar[par], r));
-        mbar_wait_cluster(&xbar[par], static_cast<uint32_t>((it >> 1) & 1), a.status);
+      }
+      aborted = __shfl_sync(0xffffffffu, aborted ? 1 : 0, 0) != 0;
+      if (aborted) {
+        if (lane == 0) {
+          if constexpr (kScore) {
+            if (rank == 0) a.logp_out[row] = __int_as_float(0x7fc00000);
+          } else {
+            sh_g[par] = 0.0f;
+            sh_lse2[par] = 0.0f;
+            sh_yl[par] = -1;
+            __threadfence_block();
+          }
+        }
+        __syncwarp();
+        if constexpr (!kScore) {
+          bar_arrive_par(kBarG, par);
+          if (lane == 0 && rank == 0) {
+            const double nan = __longlong_as_double(0x7ff8000000000000ll);
+            a.row_terms[row] = nan;
+            a.clip_mask[row] = 0;
+            if (a.logp_out != nullptr) a.logp_out[row] = __int_as_float(0x7fc00000);
+          }
+        }
+        __syncwarp();
+        continue;
+      }
+      if (lane == 0) {
         // the row's partials in rank order: the same result in every CTA of the cluster
         float M = slot[par][0][0], H = slot[par][0][1], L = slot[par][0][2];
 #pragma unroll
@@ -463,7 +506,8 @@ __global__ void __launch_bounds__(kClThreads, 4) grpo_loss_cluster(LossArgs a, i
     int it = 0;
     for (int64_t row = cid; row < R; row += ncl, ++it) {
       const uint32_t par = static_cast<uint32_t>(it & 1);
-      slice_pass1(reinterpret_cast<const uint4*>(a.logits + row * V + c0), nvec, tid, part[par]);
+      if (!*vabort)
+        slice_pass1(reinterpret_cast<const uint4*>(a.logits + row * V + c0), nvec, tid, part[par]);
       bar_arrive_par(kBarParts, par);
       bar_sync_par(kBarG, par);
       if constexpr (kScore) continue;
@@ -515,7 +559,10 @@ __global__ void __launch_bounds__(kClThreads, 4) grpo_loss_cluster(LossArgs a, i
     }
   }
   __syncwarp();
-  cluster_sync_all();   // no CTA leaves while a peer may still write its shared memory
+  // No CTA leaves while a peer may still write its shared memory.  Every wait before this
+  // point is bounded (and after an abort no CTA waits on a peer any more), so every thread
+  // of the cluster reaches this barrier in bounded time.
+  cluster_sync_all();
 }
 
 constexpr int kReduceThreads = 1024;

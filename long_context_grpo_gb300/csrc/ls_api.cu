@@ -171,14 +171,9 @@ int num_sms() {
 }
 
 // Accessors for other translation units of the library (no change to any entry point).
-int device_status_word(uint32_t** out) {
-  int dev = 0;
-  ls_status st = current_device(&dev);
-  if (st != LS_OK) return st;
-  return status_ptr(dev, out);
-}
-
 void set_last_error(const char* msg) { snprintf(t_last_error, sizeof(t_last_error), "%s", msg); }
+
+int launch_failed(cudaError_t e, const char* what) { return cuda_fail(e, what); }
 
 }  // namespace ls
 
@@ -212,6 +207,14 @@ ls_status enter(ls_prefix_t h, void* stream, uint32_t** status) {
   if (st != LS_OK) return st;
   return status_ptr(dev, status);
 }
+
+}  // namespace
+
+namespace ls {
+int enter_call(void* stream, uint32_t** status) { return enter(nullptr, stream, status); }
+}  // namespace ls
+
+namespace {
 
 // Rows [row0, ...) of a prefix-shaped bf16 [P, Hkv, D] buffer.
 const void* block_rows(ls_prefix_t h, const void* base, int64_t row0) {

@@ -151,9 +151,13 @@ inline int cached_device_index() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDeviceCache) return -1;
   return dev;
 }
-// Status word of the current device (returns an ls_status value) and the per-thread
-// message behind ls_last_error(); both live in ls_api.cu.
-int device_status_word(uint32_t** out);
+// The per-thread message behind ls_last_error() (lives in ls_api.cu).
 void set_last_error(const char* msg);
+// The checks every handle-free entry point makes before it enqueues work: the current
+// device is usable and `stream` (NULL = legacy default) belongs to it; *status receives the
+// device's status word.  Returns an ls_status value.
+int enter_call(void* stream, uint32_t** status);
+// Records the CUDA message of a failed launch for ls_last_error(); returns LS_ERR_CUDA.
+int launch_failed(cudaError_t e, const char* what);
 
 }  // namespace ls

@@ -13,8 +13,8 @@
 // (kNoAllocMaxRows doubles = 512 KB) until the process exits, and every call on a device
 // shares it.  Calls whose kernels overlap on the GPU (different streams, or different host
 // threads, without ordering between them) race on it; calls ordered on one stream do not.
-// Every row term a call reads is written earlier by the same call, so nothing needs to be
-// cleared between calls.
+// Every row term a call reads is written earlier by the same call (a row whose cluster
+// exchange gave up a bounded wait writes NaN), so nothing needs to be cleared between calls.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -85,11 +85,13 @@ extern "C" ls_status ls_grpo_loss_noalloc(int64_t R, int64_t V, int32_t G, const
       !aligned_to(logp_old, 4) || !aligned_to(loss_accum, 8) ||
       (logp_out != nullptr && !aligned_to(logp_out, 4)))
     return LS_ERR_MISALIGNED;
-  double* scratch = nullptr;
-  ls_status st = scratch_address(&scratch);
-  if (st != LS_OK) return st;
+  // the same device and stream checks as ls_grpo_loss, before the scratch address of the
+  // current device is looked up
   uint32_t* status = nullptr;
-  st = static_cast<ls_status>(device_status_word(&status));
+  ls_status st = static_cast<ls_status>(enter_call(stream, &status));
+  if (st != LS_OK) return st;
+  double* scratch = nullptr;
+  st = scratch_address(&scratch);
   if (st != LS_OK) return st;
   LossArgs a{};
   a.R = R;
@@ -107,9 +109,6 @@ extern "C" ls_status ls_grpo_loss_noalloc(int64_t R, int64_t V, int32_t G, const
   a.row_terms = scratch;
   a.status = status;
   cudaError_t e = launch_grpo_loss(a, static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) {
-    set_last_error(cudaGetErrorString(e));
-    return LS_ERR_CUDA;
-  }
+  if (e != cudaSuccess) return static_cast<ls_status>(launch_failed(e, "grpo loss (no-allocation) launch"));
   return LS_OK;
 }

@@ -179,6 +179,9 @@ __device__ __forceinline__ uint32_t cluster_map(const void* local, uint32_t rank
 __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
 // Arrive (release, cluster scope) on an mbarrier given by its shared::cluster address.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
@@ -201,6 +204,30 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
     if ((i & 63u) == 63u && globaltimer_ns() - t0 > LS_WAIT_LIMIT_NS) {
       set_device_status(status, DEV_WAIT_TIMEOUT);
       return false;
+    }
+  }
+}
+// As above, but also gives up (without recording a timeout) once *abort is set, locally or
+// by a peer CTA through distributed shared memory.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                                  volatile int* abort) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0;; ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if ((i & 63u) == 63u) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > LS_WAIT_LIMIT_NS) {
+        set_device_status(status, DEV_WAIT_TIMEOUT);
+        return false;
+      }
     }
   }
 }

@@ -32,13 +32,15 @@ Pins (tests/test_oracle_attention.py): central finite differences of <O, dO>, to
 autograd on one packed prompt+all-responses sequence with a block mask (the shared
 prefix tree), scaled_dot_product_attention in fp64, closed forms (equal keys -> mean of
 the visible values, constant values -> that value), shift invariance of the keys and the
-sum rules over keys.
+sum rules over keys; prompt_key_grads against torch fp64 autograd of causal attention over
+each [prompt; response_i] at selected prompt rows.
 """
 from __future__ import annotations
 
 import numpy as np
 
-__all__ = ["replay_response", "replay_group", "response_rows"]
+__all__ = ["replay_response", "replay_group", "response_rows", "merge_partials",
+           "prompt_key_grads"]
 
 _ROW_CHUNK = 256
 
@@ -189,3 +191,71 @@ def merge_partials(o_parts, lse_parts):
     lse = m + np.log(total)
     o = sum(wr[..., None] / total[..., None] * orr for wr, orr in zip(w, o_parts))
     return o, lse
+
+
+def prompt_key_grads(k_prefix, v_prefix, responses, keys, scale=None, row_chunk=64):
+    """Group-summed gradient w.r.t. selected prompt keys and values, float64.
+
+    The same quantity as replay_group's dk_prefix / dv_prefix, restricted to the prompt
+    rows `keys`, for prompts too long to differentiate whole on the CPU.  The gradient of a
+    single key is written out from the same explicit formulas: for response i, query head h
+    (kv head floor(h / g)) and suffix row t,
+      forward over every key the row sees (all P prompt keys, suffix keys 0..t):
+        lse_t = log sum_j exp(s q_t . k_j),  o_t = sum_j exp(s q_t . k_j - lse_t) v_j,
+        Delta_t = sum_d dO_t,d o_t,d;
+      then for a selected prompt key j (every suffix row sees every prompt key):
+        P_tj = exp(s q_t . k_j - lse_t),  dP_tj = dO_t . v_j,  dS_tj = P_tj (dP_tj - Delta_t),
+        dk_j += s sum_t dS_tj q_t,         dv_j += sum_t P_tj dO_t,
+    summed over the query heads of the kv head and over the G responses.  Only the
+    forward touches every key, so the cost is about a third of the whole-prompt backward.
+
+    k_prefix, v_prefix [P, Hkv, D]; `responses` a sequence of (q [R,Hq,D], k_suffix,
+    v_suffix [R,Hkv,D], d_out [R,Hq,D]); keys: prompt row indices.  Returns
+    (dk [n, Hkv, D], dv [n, Hkv, D]) in the order of `keys`.  Plain torch CPU ops in
+    float64 (multithreaded elementwise work); rows are processed `row_chunk` at a time.
+    """
+    import torch
+    f64 = torch.float64
+
+    def t64(x):
+        if isinstance(x, torch.Tensor):
+            return x.detach().to("cpu", f64)
+        return torch.as_tensor(np.asarray(x, dtype=np.float64))
+
+    Kp, Vp = t64(k_prefix), t64(v_prefix)
+    P, Hkv, D = Kp.shape
+    s = (1.0 / np.sqrt(D)) if scale is None else float(scale)
+    J = torch.as_tensor(np.asarray(keys, dtype=np.int64))
+    dk = torch.zeros((len(J), Hkv, D), dtype=f64)
+    dv = torch.zeros((len(J), Hkv, D), dtype=f64)
+    for (q, ks, vs, do) in responses:
+        Q, Ks, Vs, dO = t64(q), t64(ks), t64(vs), t64(do)
+        R, Hq, _ = Q.shape
+        for h in range(Hq):
+            kv = _kv_of(h, Hq, Hkv)
+            Kh, Vh = Kp[:, kv, :], Vp[:, kv, :]
+            Ksh, Vsh = Ks[:, kv, :], Vs[:, kv, :]
+            lse = torch.empty(R, dtype=f64)
+            delta = torch.empty(R, dtype=f64)
+            for t0 in range(0, R, row_chunk):
+                t1 = min(R, t0 + row_chunk)
+                Qc = Q[t0:t1, h, :]
+                S_p = s * (Qc @ Kh.T)                                   # [c, P], all visible
+                S_s = s * (Qc @ Ksh.T)                                  # [c, R], causal
+                t = torch.arange(t0, t1)
+                S_s = torch.where(torch.arange(R)[None, :] <= t[:, None], S_s,
+                                  torch.full_like(S_s, -np.inf))
+                m = torch.maximum(S_p.amax(dim=1), S_s.amax(dim=1))[:, None]
+                E_p = torch.exp(S_p - m)
+                E_s = torch.exp(S_s - m)
+                l = E_p.sum(dim=1) + E_s.sum(dim=1)
+                o = (E_p @ Vh + E_s @ Vsh) / l[:, None]
+                lse[t0:t1] = m[:, 0] + torch.log(l)
+                delta[t0:t1] = (dO[t0:t1, h, :] * o).sum(dim=1)
+            KJ, VJ = Kh[J], Vh[J]
+            Pm = torch.exp(s * (Q[:, h, :] @ KJ.T) - lse[:, None])        # [R, n]
+            dP = dO[:, h, :] @ VJ.T
+            dS = Pm * (dP - delta[:, None])
+            dk[:, kv, :] += s * (dS.T @ Q[:, h, :])
+            dv[:, kv, :] += Pm.T @ dO[:, h, :]
+    return dk.numpy(), dv.numpy()

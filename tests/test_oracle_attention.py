@@ -225,3 +225,39 @@ def test_merge_of_key_shards_equals_attention_over_all_keys():
     o2, l2 = att.merge_partials([o_parts[0], o_parts[1]], [lse_parts[0], lse_parts[0]])
     assert np.allclose(o2, 0.5 * (o_parts[0] + o_parts[1]), atol=1e-15)
     assert np.allclose(l2, lse_parts[0] + np.log(2.0), atol=1e-15)
+
+
+@pytest.mark.parametrize("Hq,Hkv,D", [(4, 2, 5), (3, 3, 4), (6, 1, 8)])
+def test_prompt_key_grads_match_autograd_at_selected_keys(Hq, Hkv, D):
+    """prompt_key_grads against torch fp64 autograd of plain causal attention over each
+    concatenated [prompt; response_i] (explicit mask, explicit softmax), the prompt
+    gradients summed over the group, at an unsorted subset of prompt rows with a repeat."""
+    rng = np.random.default_rng(Hq * 100 + Hkv * 10 + D)
+    P, Rs = 11, [4, 1, 6]
+    g = Hq // Hkv
+    s = 1.0 / np.sqrt(D)
+    kp, vp = _rand((P, Hkv, D), rng, 0.9), _rand((P, Hkv, D), rng, 0.9)
+    resp = [(_rand((R, Hq, D), rng, 0.9), _rand((R, Hkv, D), rng, 0.9),
+             _rand((R, Hkv, D), rng, 0.9), _rand((R, Hq, D), rng)) for R in Rs]
+    Kp = torch.tensor(kp, requires_grad=True)
+    Vp = torch.tensor(vp, requires_grad=True)
+    total = 0.0
+    for q, ks, vs, do in resp:
+        R = q.shape[0]
+        K = torch.cat([Kp, torch.tensor(ks)])                     # [P+R, Hkv, D]
+        V = torch.cat([Vp, torch.tensor(vs)])
+        Q = torch.tensor(q)
+        mask = torch.arange(P + R)[None, :] <= (P + torch.arange(R))[:, None]
+        for h in range(Hq):
+            S = s * Q[:, h, :] @ K[:, h // g, :].T
+            A = torch.softmax(S.masked_fill(~mask, float("-inf")), dim=1)
+            total = total + (A @ V[:, h // g, :] * torch.tensor(do[:, h, :])).sum()
+    total.backward()
+    keys = [7, 0, P - 1, 3, 7]
+    dk, dv = att.prompt_key_grads(kp, vp, resp, keys)
+    np.testing.assert_allclose(dk, Kp.grad.numpy()[keys], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dv, Vp.grad.numpy()[keys], rtol=1e-10, atol=1e-12)
+    # small row chunks split the forward statistics across chunks: same result
+    dk2, dv2 = att.prompt_key_grads(kp, vp, resp, keys, row_chunk=2)
+    np.testing.assert_allclose(dk2, dk, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(dv2, dv, rtol=1e-12, atol=1e-14)

@@ -14,7 +14,13 @@ What the float64 oracle can afford to compute at each size:
               - for the fp32 prompt accumulators, properties that hold at any size: the
                 sum over all keys of dV equals the sum of dO over the group's rows, the sum
                 over all keys of dK vanishes, and the prompt K/V are bit-identical after the
-                replay.
+                replay;
+              - the fp32 prompt accumulators element by element at 512+ seeded prompt
+                positions (the first and last prompt tiles among them) of one kv head, on a
+                fresh handle over the full prompt with two short ragged responses, against
+                the oracle's per-key gradient (oracle.prompt_key_grads), through the whole
+                call sequence (prepare, fwd, bwd, bf16 finalize with scale 1/G); also on a
+                prompt 1,000 rows past 2M (a ragged last tile, element offsets past 2^31).
 """
 import numpy as np
 import pytest
@@ -235,3 +241,75 @@ def test_peak_memory_is_flat_in_group_size():
 
     p2, p8 = peak(2), peak(8)
     assert p8 - p2 <= per_resp, (p2, p8, per_resp)
+
+
+# --------------------------------------------------------------------------- prompt gradients
+PROMPT_GRAD_R = (300, 77)
+# (workload, prompt rows, kv head checked): never kv head 0, so a head offset cannot hide; on
+# the prompt past 2M the last kv head puts elements (row * Hkv + kv) * D beyond 2^31.
+PROMPT_GRAD_CASES = [("p262k", 262144, 5), ("p1m", 1048576, 3), ("p2m", 2097152, 6),
+                     ("p2m", 2097152 + 1000, 7)]
+
+
+def _sampled_positions(P, rng, n_random=256):
+    """The first and the last prompt tiles (the last one ragged when P % 128 != 0) and
+    n_random seeded positions in between."""
+    first = np.arange(0, 128)
+    last = np.arange((P - 1) // 128 * 128, P)
+    mid = np.sort(rng.choice(np.arange(128, (P - 1) // 128 * 128), n_random, replace=False))
+    return first, mid, last
+
+
+@pytest.mark.parametrize("name,P,kv", PROMPT_GRAD_CASES,
+                         ids=["p262k", "p1m", "p2m", "p2m_plus_1000"])
+def test_large_config_prompt_gradients_at_sampled_positions(name, P, kv):
+    import long_context_grpo_gb300 as ls
+    _CACHE.clear()
+    torch.cuda.empty_cache()
+    w = wl.WORKLOADS[name]
+    g = w.group
+    kp, vp = wl.prefix_kv(w, 0, "cuda", P=P)
+    resp = [wl.response_attention(w, i, R, 0, "cuda") for i, R in enumerate(PROMPT_GRAD_R)]
+    dk_acc = torch.empty((P, w.Hkv, w.D), dtype=torch.float32, device="cuda")
+    dv_acc = torch.empty_like(dk_acc)
+    pre = ls.Prefix(kp, vp, dk_acc, dv_acc, Hq=w.Hq)
+    outs = []
+    for (q, ks, vs, do) in resp:
+        o, lse = pre.fwd(q, ks, vs)
+        outs.append(pre.bwd(q, ks, vs, o, lse, do))
+    scale = 1.0 / len(resp)
+    dk_out = torch.empty(dk_acc.shape, dtype=torch.bfloat16, device="cuda")
+    dv_out = torch.empty_like(dk_out)
+    pre.finalize(scale, dk_out, dv_out)
+    torch.cuda.synchronize()
+    assert ls.device_status() == (0, 0)
+    pre.close()
+
+    first, mid, last = _sampled_positions(P, np.random.default_rng(P + kv))
+    keys = np.concatenate([first, mid, last])
+    hs = slice(kv * g, (kv + 1) * g)
+    sl = [(q[:, hs].cpu(), ks[:, kv:kv + 1].cpu(), vs[:, kv:kv + 1].cpu(), do[:, hs].cpu())
+          for (q, ks, vs, do) in resp]
+    dk_ref, dv_ref = oracle.prompt_key_grads(kp[:, kv:kv + 1].cpu(), vp[:, kv:kv + 1].cpu(),
+                                             sl, keys)
+    idx = torch.tensor(keys, device="cuda")
+    got_k = dk_acc.index_select(0, idx)[:, kv:kv + 1]
+    got_v = dv_acc.index_select(0, idx)[:, kv:kv + 1]
+    n1, n2 = len(first), len(first) + len(mid)
+    for part, sel in (("first tile", slice(0, n1)), ("random", slice(n1, n2)),
+                      ("last tile", slice(n2, None)), ("all", slice(None))):
+        assert rel_l2(got_k[sel], dk_ref[sel]) < TOL_PREFIX, (name, P, "dk", part)
+        assert rel_l2(got_v[sel], dv_ref[sel]) < TOL_PREFIX, (name, P, "dv", part)
+    # the finalized bf16 gradient the benchmark produces: scale * the group sum
+    fin_k = dk_out.index_select(0, idx)[:, kv:kv + 1]
+    fin_v = dv_out.index_select(0, idx)[:, kv:kv + 1]
+    assert rel_l2(fin_k, scale * dk_ref) < TOL_PREFIX, (name, P, "finalized dk")
+    assert rel_l2(fin_v, scale * dv_ref) < TOL_PREFIX, (name, P, "finalized dv")
+    # any size: the sum rules over every key of the group (prompt + both suffixes)
+    dv_sum = dv_acc.double().sum(dim=0)
+    want = torch.zeros_like(dv_sum)
+    for (dq, dks, dvs), (q, ks, vs, do) in zip(outs, resp):
+        dv_sum += dvs.double().sum(dim=0)
+        want += do.double().view(do.shape[0], w.Hkv, g, w.D).sum(dim=(0, 2))
+    assert rel_l2(dv_sum, want) < TOL_PREFIX, (name, P)
+    del kp, vp, dk_acc, dv_acc, dk_out, dv_out
