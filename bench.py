@@ -617,7 +617,7 @@ def kernel_table(kt, work, steps, total_ms, peaks):
     the measured peak of its bound (sustained bf16 for contractions, HBM copy otherwise)."""
     kernels = {}
     for name, (tot_ms, n) in kt.items():
-        if n == 0 or tot_ms <= 0:
+        if n == 0 or tot_ms <= 0 or name not in work:
             continue
         amount, unit = work[name]
         per_launch_amount = amount * steps / n

@@ -302,6 +302,11 @@ int64_t ls_grpo_loss_noalloc_max_rows(void);
  *
  * ls_sum_bf16: out[i] = bf16(sum_r float(parts[r][i])), 0 <= i < count; parts a HOST array
  *   of n device pointers (bf16); 1 <= n <= 16, count a multiple of 8.
+ *
+ * ls_bf16_to_f32 / ls_f32_to_bf16: the element conversions around the cross-rank fp32 sum
+ *   of the dq parts (each rank widens its bf16 part exactly, the collective sums in fp32,
+ *   the sum is rounded back to bf16 to nearest, ties to even).  count values (a multiple of
+ *   8, else LS_ERR_UNSUPPORTED); in and out device, 16-byte aligned, not overlapping.
  */
 ls_status ls_replay_fwd_prompt_only(ls_prefix_t h, int64_t R, const void* q, void* o, float* lse,
                                     void* stream);
@@ -311,6 +316,8 @@ ls_status ls_replay_bwd_prompt_only(ls_prefix_t h, int64_t R, const void* q, con
 ls_status ls_attn_merge(int32_t n, int64_t R, int32_t Hq, int32_t D, const void* const* o_parts,
                         const float* const* lse_parts, void* o, float* lse, void* stream);
 ls_status ls_sum_bf16(int32_t n, int64_t count, const void* const* parts, void* out, void* stream);
+ls_status ls_bf16_to_f32(int64_t count, const void* in, float* out, void* stream);
+ls_status ls_f32_to_bf16(int64_t count, const float* in, void* out, void* stream);
 
 /*
  * ls_prefix_grad_finalize -- the group's one finalization (review section 2-1 step 5;
@@ -360,7 +367,8 @@ typedef enum {
   LS_KERNEL_TOKEN_LOGP = 7,    /* scoring: token log-prob only                    */
   LS_KERNEL_MERGE = 8,         /* context-parallel partial-attention merge        */
   LS_KERNEL_SUM = 9,           /* context-parallel dQ part sum                    */
-  LS_KERNEL_COUNT = 10
+  LS_KERNEL_CAST = 10,         /* context-parallel bf16 <-> fp32 conversions      */
+  LS_KERNEL_COUNT = 11
 } ls_kernel_id;
 
 ls_status ls_timing_enable(int enable);

@@ -8,7 +8,7 @@ __version__ = "0.1.0"
 
 _BINDING = ("Prefix", "grpo_loss", "grpo_loss_workspace_bytes", "device_status",
             "LongStrawError", "library_path", "STATUS_NAMES", "timing_enable", "timing_read", "token_logp",
-            "KERNEL_NAMES", "attn_merge", "sum_bf16")
+            "KERNEL_NAMES", "attn_merge", "sum_bf16", "bf16_to_f32", "f32_to_bf16")
 
 
 def __getattr__(name):

@@ -69,6 +69,8 @@ def _load():
         "ls_replay_bwd_prompt_only": (ctypes.c_int, [vp, i64, vp, vp, vp, vp, vp, vp, sz, vp]),
         "ls_attn_merge": (ctypes.c_int, [i32, i64, i32, i32, vp, vp, vp, vp, vp]),
         "ls_sum_bf16": (ctypes.c_int, [i32, i64, vp, vp, vp]),
+        "ls_bf16_to_f32": (ctypes.c_int, [i64, vp, vp, vp]),
+        "ls_f32_to_bf16": (ctypes.c_int, [i64, vp, vp, vp]),
         "ls_replay_bwd_packed_workspace_bytes": (sz, [vp, i32, vp]),
         "ls_replay_bwd_packed": (ctypes.c_int, [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                                 vp, sz, vp]),
@@ -358,6 +360,24 @@ def sum_bf16(parts, out=None):
     return out
 
 
+def bf16_to_f32(x, out=None):
+    """Exact widening of a bf16 tensor to fp32 (numel a multiple of 8)."""
+    out = torch.empty(x.shape, dtype=torch.float32, device=x.device) if out is None else out
+    _check(_lib().ls_bf16_to_f32(x.numel(), _ptr(x, "x", torch.bfloat16),
+                                 _ptr(out, "out", torch.float32, tuple(x.shape)), _stream()),
+           "ls_bf16_to_f32")
+    return out
+
+
+def f32_to_bf16(x, out=None):
+    """fp32 -> bf16, round to nearest, ties to even (numel a multiple of 8)."""
+    out = torch.empty(x.shape, dtype=torch.bfloat16, device=x.device) if out is None else out
+    _check(_lib().ls_f32_to_bf16(x.numel(), _ptr(x, "x", torch.float32),
+                                 _ptr(out, "out", torch.bfloat16, tuple(x.shape)), _stream()),
+           "ls_f32_to_bf16")
+    return out
+
+
 def grpo_loss_workspace_bytes(R: int) -> int:
     return int(_lib().ls_grpo_loss_workspace_bytes(R))
 
@@ -385,7 +405,7 @@ def grpo_loss(logits, ids, logp_old, advantage: float, eps: float, G: int, loss_
 
 
 KERNEL_NAMES = ("zero", "replay_fwd", "bwd_prep", "bwd_dkdv", "bwd_dq", "grpo_loss", "finalize",
-                "token_logp", "merge", "sum")
+                "token_logp", "merge", "sum", "cast")
 
 
 def timing_enable(on: bool = True):

@@ -8,6 +8,7 @@
 //                      lse = log sum_r exp(lse_r), o = sum_r exp(lse_r - lse) o_r
 //                      (LongStraw review, section 3-2 (2): global LSE/output merge)
 //   sum_bf16           sum of per-shard dQ partials, fp32 accumulation, bf16 out
+//   bf16 <-> f32       conversions around the cross-rank fp32 sum of the dQ parts
 // All use 128-bit accesses on a grid sized to the SM count.
 #include "ls_internal.h"
 #include "ptx.cuh"
@@ -166,6 +167,34 @@ __global__ void __launch_bounds__(kThreads) sum_bf16_kernel(const __grid_constan
   }
 }
 
+// Element-type conversions of the context-parallel dQ exchange: the bf16 dQ part of a
+// shard is summed across ranks in fp32 (8 values per thread, 128-bit accesses).
+__global__ void __launch_bounds__(kThreads) bf16_to_f32_kernel(const uint4* in, float4* out,
+                                                              size_t n8) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * kThreads;
+  for (size_t i = blockIdx.x * static_cast<size_t>(kThreads) + threadIdx.x; i < n8; i += stride) {
+    const uint4 v = __ldcs(in + i);
+    __stcs(out + 2 * i, make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u),
+                                    __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u)));
+    __stcs(out + 2 * i + 1, make_float4(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xFFFF0000u),
+                                        __uint_as_float(v.w << 16), __uint_as_float(v.w & 0xFFFF0000u)));
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) f32_to_bf16_kernel(const float4* in, uint4* out,
+                                                              size_t n8) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * kThreads;
+  for (size_t i = blockIdx.x * static_cast<size_t>(kThreads) + threadIdx.x; i < n8; i += stride) {
+    const float4 a = __ldcs(in + 2 * i), b = __ldcs(in + 2 * i + 1);
+    uint4 o;
+    o.x = bf16x2_rn(a.x, a.y);
+    o.y = bf16x2_rn(a.z, a.w);
+    o.z = bf16x2_rn(b.x, b.y);
+    o.w = bf16x2_rn(b.z, b.w);
+    __stcs(out + i, o);
+  }
+}
+
 // Failure-detection self test: one thread waits on an mbarrier that nothing arrives at,
 // bounded by limit_ns, then records DEV_WAIT_TIMEOUT exactly as the replay kernels do when
 // a wait gives up, and exits; the context stays usable.
@@ -226,6 +255,18 @@ cudaError_t launch_attn_merge(const MergeArgs& a, cudaStream_t s) {
 
 cudaError_t launch_sum_bf16(const SumArgs& a, cudaStream_t s) {
   sum_bf16_kernel<<<grid_for(static_cast<size_t>(a.count / 8)), kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bf16_to_f32(const void* in, float* out, size_t count, cudaStream_t s) {
+  bf16_to_f32_kernel<<<grid_for(count / 8), kThreads, 0, s>>>(static_cast<const uint4*>(in),
+                                                             reinterpret_cast<float4*>(out), count / 8);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_f32_to_bf16(const float* in, void* out, size_t count, cudaStream_t s) {
+  f32_to_bf16_kernel<<<grid_for(count / 8), kThreads, 0, s>>>(reinterpret_cast<const float4*>(in),
+                                                             static_cast<uint4*>(out), count / 8);
   return cudaGetLastError();
 }
 

@@ -707,6 +707,36 @@ ls_status ls_sum_bf16(int32_t n, int64_t count, const void* const* parts, void* 
   return e == cudaSuccess ? LS_OK : cuda_fail(e, "sum launch");
 }
 
+ls_status ls_bf16_to_f32(int64_t count, const void* in, float* out, void* stream) {
+  if (in == nullptr || out == nullptr || count < 1) return LS_ERR_INVALID_ARGUMENT;
+  if (count % 8 != 0) return LS_ERR_UNSUPPORTED;
+  if (!aligned16(in) || !aligned16(out)) return LS_ERR_MISALIGNED;
+  uint32_t* status = nullptr;
+  ls_status st = enter(nullptr, stream, &status);
+  if (st != LS_OK) return st;
+  cudaError_t e;
+  {
+    LaunchTimer t(LS_KERNEL_CAST, static_cast<cudaStream_t>(stream));
+    e = launch_bf16_to_f32(in, out, static_cast<size_t>(count), static_cast<cudaStream_t>(stream));
+  }
+  return e == cudaSuccess ? LS_OK : cuda_fail(e, "bf16 -> fp32 launch");
+}
+
+ls_status ls_f32_to_bf16(int64_t count, const float* in, void* out, void* stream) {
+  if (in == nullptr || out == nullptr || count < 1) return LS_ERR_INVALID_ARGUMENT;
+  if (count % 8 != 0) return LS_ERR_UNSUPPORTED;
+  if (!aligned16(in) || !aligned16(out)) return LS_ERR_MISALIGNED;
+  uint32_t* status = nullptr;
+  ls_status st = enter(nullptr, stream, &status);
+  if (st != LS_OK) return st;
+  cudaError_t e;
+  {
+    LaunchTimer t(LS_KERNEL_CAST, static_cast<cudaStream_t>(stream));
+    e = launch_f32_to_bf16(in, out, static_cast<size_t>(count), static_cast<cudaStream_t>(stream));
+  }
+  return e == cudaSuccess ? LS_OK : cuda_fail(e, "fp32 -> bf16 launch");
+}
+
 ls_status ls_prefix_grad_finalize(ls_prefix_t h, float scale, void* dk_out, void* dv_out,
                                   int out_is_fp32, int reset_acc, void* stream) {
   ls_status st = check_handle(h);

@@ -55,6 +55,10 @@ struct SumArgs {
 };
 cudaError_t launch_sum_bf16(const SumArgs& a, cudaStream_t s);
 cudaError_t launch_scale_inplace(float* acc, size_t n, float scale, cudaStream_t s);
+// Exact bf16 -> fp32 widening and fp32 -> bf16 rounding (nearest, ties to even) of count
+// values (a multiple of 8, 16-byte aligned buffers).
+cudaError_t launch_bf16_to_f32(const void* in, float* out, size_t count, cudaStream_t s);
+cudaError_t launch_f32_to_bf16(const float* in, void* out, size_t count, cudaStream_t s);
 
 // ----- attention (k_attn_fwd.cu, k_attn_bwd.cu)
 struct AttnShape {

@@ -146,3 +146,24 @@ def test_rank_driver_with_a_one_rank_group():
     assert np.max(np.abs(f64(lse) - ref["lse"])) < TOL_LSE
     assert rel_l2(dks, ref["dk_suffix"]) < TOL_BF16 and rel_l2(dvs, ref["dv_suffix"]) < TOL_BF16
     assert rel_l2(dkf, ref["dk_prefix"]) < TOL_PREFIX and rel_l2(dvf, ref["dv_prefix"]) < TOL_PREFIX
+
+
+def test_dq_exchange_conversions_against_the_oracle_rounding():
+    """ls_bf16_to_f32 widens exactly; ls_f32_to_bf16 rounds to nearest, ties to even, bit
+    for bit as oracle.numerics.to_bf16 (values across the exponent range, ties included)."""
+    import long_context_grpo_gb300 as ls
+    from oracle.numerics import to_bf16
+    g = torch.Generator(device="cpu").manual_seed(21)
+    bits = torch.randint(0, 2 ** 31 - 1, (4096,), generator=g, dtype=torch.int64)
+    bits[::2] |= 0x8000                                 # half of the low halves at a tie
+    x = (bits.to(torch.int32)).view(torch.float32)
+    x = torch.where(torch.isfinite(x), x, torch.zeros_like(x))
+    x = torch.cat([x, -x])
+    got = ls.f32_to_bf16(x.cuda())
+    want = to_bf16(x.double().numpy())
+    assert np.array_equal(f64(got), want)
+    back = ls.bf16_to_f32(got)
+    torch.cuda.synchronize()
+    assert np.array_equal(f64(back), want)
+    with pytest.raises(ls.LongStrawError):
+        ls.f32_to_bf16(torch.zeros(12, device="cuda"))   # count % 8
