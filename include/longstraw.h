@@ -384,6 +384,20 @@ ls_status ls_timing_read(double* total_ms, int64_t* launches, int n);
  */
 ls_status ls_debug_wait_timeout(uint64_t limit_ns, void* stream);
 
+/*
+ * Launch-failure injection (test aid for the error paths; no GPU fault is involved).
+ * ls_debug_fail_launch(after) arms a countdown of the library's launch attempts: the next
+ * `after` attempts launch normally and the one after them is not made -- the entry point
+ * making it returns LS_ERR_CUDA with "launch failure injected" in ls_last_error(), exactly
+ * as for a real launch error, and the countdown disarms.  after < 0 disarms it.  A call that
+ * launches several kernels (ls_replay_bwd: prep, dK/dV, dQ; the two halves of the zeroing and
+ * of the finalization) counts each as one attempt, so a failure can be placed between them.
+ * Calls rejected by their argument checks make no attempt and do not consume the countdown.
+ * ls_debug_fail_launch_pending() returns the countdown (-1 when disarmed).  Process-wide.
+ */
+ls_status ls_debug_fail_launch(int64_t after);
+int64_t ls_debug_fail_launch_pending(void);
+
 const char* ls_status_string(ls_status s);
 
 /* Message of the last CUDA failure seen by this thread ("" if none). */

@@ -78,6 +78,8 @@ def _load():
         "ls_get_device_status": (ctypes.c_int, [vp, ctypes.POINTER(ctypes.c_uint32)]),
         "ls_timing_enable": (ctypes.c_int, [ctypes.c_int]),
         "ls_debug_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, vp]),
+        "ls_debug_fail_launch": (ctypes.c_int, [i64]),
+        "ls_debug_fail_launch_pending": (i64, []),
         "ls_timing_read": (ctypes.c_int, [ctypes.POINTER(ctypes.c_double),
                                           ctypes.POINTER(ctypes.c_int64), ctypes.c_int]),
         "ls_status_string": (ctypes.c_char_p, [ctypes.c_int]),

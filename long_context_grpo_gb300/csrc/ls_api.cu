@@ -6,6 +6,9 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <nvtx3/nvToolsExt.h>
+
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -20,6 +23,23 @@
 namespace ls {
 
 __device__ uint32_t g_status_word = 0u;
+
+// ----- launch-failure injection (ls_debug_fail_launch): a countdown of launch attempts;
+// the attempt that finds it at 0 is not made and reports LS_ERR_CUDA.
+std::atomic<int64_t> g_fail_countdown{-1};
+thread_local bool t_injected = false;
+
+bool injected_failure() {
+  int64_t c = g_fail_countdown.load();
+  while (c >= 0) {
+    if (g_fail_countdown.compare_exchange_weak(c, c - 1)) {
+      if (c != 0) return false;
+      t_injected = true;
+      return true;
+    }
+  }
+  return false;
+}
 
 namespace {
 
@@ -36,9 +56,21 @@ uint32_t* g_status_ptr[kMaxDevices] = {};
 int g_num_sms[kMaxDevices] = {};
 
 ls_status cuda_fail(cudaError_t e, const char* what) {
+  if (t_injected) {
+    t_injected = false;
+    snprintf(t_last_error, sizeof(t_last_error), "%s: launch failure injected by ls_debug_fail_launch",
+             what);
+    return LS_ERR_CUDA;
+  }
   snprintf(t_last_error, sizeof(t_last_error), "%s: %s", what, cudaGetErrorString(e));
   return LS_ERR_CUDA;
 }
+
+// One NVTX range per API call (visible to profilers; no-op without one attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0u; }
 bool aligned_n(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0u; }
@@ -281,7 +313,7 @@ ls_status replay_fwd_impl(ls_prefix_t h, int64_t P_eff, int32_t G, const int64_t
   cudaError_t e;
   {
     LaunchTimer t(LS_KERNEL_REPLAY_FWD, static_cast<cudaStream_t>(stream));
-    e = launch_attn_fwd(a, static_cast<cudaStream_t>(stream));
+    e = injected_failure() ? cudaErrorLaunchFailure : launch_attn_fwd(a, static_cast<cudaStream_t>(stream));
   }
   return e == cudaSuccess ? LS_OK : cuda_fail(e, "replay forward launch");
 }
@@ -342,18 +374,18 @@ ls_status replay_bwd_impl(ls_prefix_t h, int64_t P_eff, int32_t G, const int64_t
   cudaError_t e;
   {
     LaunchTimer t(LS_KERNEL_BWD_PREP, s);
-    e = launch_bwd_prep(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(d_out), lse,
+    e = injected_failure() ? cudaErrorLaunchFailure : launch_bwd_prep(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(d_out), lse,
                         rowstats, sh, a.vl, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "replay backward prep launch");
   {
     LaunchTimer t(LS_KERNEL_BWD_DKDV, s);
-    e = launch_attn_bwd_dkdv(a, s);
+    e = injected_failure() ? cudaErrorLaunchFailure : launch_attn_bwd_dkdv(a, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "replay backward dK/dV launch");
   {
     LaunchTimer t(LS_KERNEL_BWD_DQ, s);
-    e = launch_attn_bwd_dq(a, s);
+    e = injected_failure() ? cudaErrorLaunchFailure : launch_attn_bwd_dq(a, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "replay backward dQ launch");
   return LS_OK;
@@ -379,12 +411,12 @@ ls_status finalize_impl(ls_prefix_t h, int64_t row0, int64_t nrows, float scale,
   cudaError_t e;
   LaunchTimer t(LS_KERNEL_FINALIZE, s);
   if (inplace) {
-    e = launch_scale_inplace(dk, n, scale, s);
-    if (e == cudaSuccess) e = launch_scale_inplace(dv, n, scale, s);
+    e = injected_failure() ? cudaErrorLaunchFailure : launch_scale_inplace(dk, n, scale, s);
+    if (e == cudaSuccess) e = injected_failure() ? cudaErrorLaunchFailure : launch_scale_inplace(dv, n, scale, s);
   } else {
-    e = launch_finalize(dk, dk_out, n, scale, out_is_fp32 ? 1 : 0, reset_acc ? 1 : 0, s);
+    e = injected_failure() ? cudaErrorLaunchFailure : launch_finalize(dk, dk_out, n, scale, out_is_fp32 ? 1 : 0, reset_acc ? 1 : 0, s);
     if (e == cudaSuccess)
-      e = launch_finalize(dv, dv_out, n, scale, out_is_fp32 ? 1 : 0, reset_acc ? 1 : 0, s);
+      e = injected_failure() ? cudaErrorLaunchFailure : launch_finalize(dv, dv_out, n, scale, out_is_fp32 ? 1 : 0, reset_acc ? 1 : 0, s);
   }
   return e == cudaSuccess ? LS_OK : cuda_fail(e, "finalize launch");
 }
@@ -414,6 +446,7 @@ const char* ls_status_string(ls_status s) {
 }
 
 ls_status ls_prefix_prepare(const ls_prefix_desc* d, ls_prefix_t* out, void* stream) {
+  NvtxRange nvtx_range("ls_prefix_prepare");
   if (d == nullptr || out == nullptr) return LS_ERR_INVALID_ARGUMENT;
   if (d->k_prefix == nullptr || d->v_prefix == nullptr || d->dk_acc == nullptr ||
       d->dv_acc == nullptr)
@@ -463,8 +496,8 @@ ls_status ls_prefix_prepare(const ls_prefix_desc* d, ls_prefix_t* out, void* str
   cudaError_t e;
   {
     LaunchTimer t(LS_KERNEL_ZERO, s);
-    e = launch_zero_f32(d->dk_acc, n, s);
-    if (e == cudaSuccess) e = launch_zero_f32(d->dv_acc, n, s);
+    e = injected_failure() ? cudaErrorLaunchFailure : launch_zero_f32(d->dk_acc, n, s);
+    if (e == cudaSuccess) e = injected_failure() ? cudaErrorLaunchFailure : launch_zero_f32(d->dv_acc, n, s);
   }
   if (e != cudaSuccess) {
     delete h;
@@ -485,6 +518,7 @@ ls_status ls_prefix_destroy(ls_prefix_t h) {
 
 ls_status ls_replay_fwd(ls_prefix_t h, int64_t R, const void* q, const void* k_suffix,
                         const void* v_suffix, void* o, float* lse, void* stream) {
+  NvtxRange nvtx_range("ls_replay_fwd");
   ls_status st = check_handle(h);
   if (st != LS_OK) return st;
   const int64_t cu[2] = {0, R};
@@ -495,6 +529,7 @@ ls_status ls_replay_fwd(ls_prefix_t h, int64_t R, const void* q, const void* k_s
 ls_status ls_replay_fwd_packed(ls_prefix_t h, int32_t G, const int64_t* cu_seqlens,
                                const void* q, const void* k_suffix, const void* v_suffix,
                                void* o, float* lse, void* stream) {
+  NvtxRange nvtx_range("ls_replay_fwd_packed");
   ls_status st = check_handle(h);
   if (st != LS_OK) return st;
   return replay_fwd_impl(h, h->shape.P, G, cu_seqlens, q, k_suffix, v_suffix, o, lse, stream);
@@ -502,6 +537,7 @@ ls_status ls_replay_fwd_packed(ls_prefix_t h, int32_t G, const int64_t* cu_seqle
 
 ls_status ls_block_replay_fwd(ls_prefix_t h, int64_t prefix_len, int64_t R, const void* q,
                               void* o, float* lse, void* stream) {
+  NvtxRange nvtx_range("ls_block_replay_fwd");
   ls_status st = check_handle(h);
   if (st != LS_OK) return st;
   if (prefix_len < 1 || R < 1 || prefix_len > h->shape.P - R) return LS_ERR_INVALID_ARGUMENT;
@@ -520,6 +556,7 @@ ls_status ls_replay_bwd(ls_prefix_t h, int64_t R, const void* q, const void* k_s
                         const void* v_suffix, const void* o, const float* lse,
                         const void* d_out, void* dq, void* dk_suffix, void* dv_suffix,
                         void* workspace, size_t workspace_bytes, void* stream) {
+  NvtxRange nvtx_range("ls_replay_bwd");
   ls_status st = check_handle(h);
   if (st != LS_OK) return st;
   if (dk_suffix == nullptr || dv_suffix == nullptr) return LS_ERR_INVALID_ARGUMENT;
@@ -540,6 +577,7 @@ ls_status ls_replay_bwd_packed(ls_prefix_t h, int32_t G, const int64_t* cu_seqle
                                const void* o, const float* lse, const void* d_out, void* dq,
                                void* dk_suffix, void* dv_suffix, void* workspace,
                                size_t workspace_bytes, void* stream) {
+  NvtxRange nvtx_range("ls_replay_bwd_packed");
   ls_status st = check_handle(h);
   if (st != LS_OK) return st;
   if (dk_suffix == nullptr || dv_suffix == nullptr) return LS_ERR_INVALID_ARGUMENT;
@@ -551,6 +589,7 @@ ls_status ls_replay_bwd_packed(ls_prefix_t h, int32_t G, const int64_t* cu_seqle
 ls_status ls_block_replay_bwd(ls_prefix_t h, int64_t prefix_len, int64_t R, const void* q,
                               const void* o, const float* lse, const void* d_out, void* dq,
                               void* workspace, size_t workspace_bytes, void* stream) {
+  NvtxRange nvtx_range("ls_block_replay_bwd");
   ls_status st = check_handle(h);
   if (st != LS_OK) return st;
   if (prefix_len < 1 || R < 1 || prefix_len > h->shape.P - R) return LS_ERR_INVALID_ARGUMENT;
@@ -569,6 +608,7 @@ ls_status ls_grpo_loss(int64_t R, int64_t V, int32_t G, const void* logits, cons
                        const float* logp_old, double advantage, double eps, double* loss_accum,
                        void* dlogits, uint8_t* clip_mask, float* logp_out, void* workspace,
                        size_t workspace_bytes, void* stream) {
+  NvtxRange nvtx_range("ls_grpo_loss");
   if (logits == nullptr || ids == nullptr || logp_old == nullptr || loss_accum == nullptr ||
       dlogits == nullptr || clip_mask == nullptr)
     return LS_ERR_INVALID_ARGUMENT;
@@ -602,13 +642,14 @@ ls_status ls_grpo_loss(int64_t R, int64_t V, int32_t G, const void* logits, cons
   cudaError_t e;
   {
     LaunchTimer t(LS_KERNEL_GRPO_LOSS, static_cast<cudaStream_t>(stream));
-    e = launch_grpo_loss(a, static_cast<cudaStream_t>(stream));
+    e = injected_failure() ? cudaErrorLaunchFailure : launch_grpo_loss(a, static_cast<cudaStream_t>(stream));
   }
   return e == cudaSuccess ? LS_OK : cuda_fail(e, "grpo loss launch");
 }
 
 ls_status ls_token_logp(int64_t R, int64_t V, const void* logits, const int32_t* ids,
                         float* logp_out, void* stream) {
+  NvtxRange nvtx_range("ls_token_logp");
   if (logits == nullptr || ids == nullptr || logp_out == nullptr) return LS_ERR_INVALID_ARGUMENT;
   if (R < 1 || V < 1) return LS_ERR_INVALID_ARGUMENT;
   if (R >= (int64_t(1) << 31) || V >= (int64_t(1) << 31)) return LS_ERR_UNSUPPORTED;
@@ -628,13 +669,14 @@ ls_status ls_token_logp(int64_t R, int64_t V, const void* logits, const int32_t*
   cudaError_t e;
   {
     LaunchTimer t(LS_KERNEL_TOKEN_LOGP, static_cast<cudaStream_t>(stream));
-    e = launch_token_logp(a, static_cast<cudaStream_t>(stream));
+    e = injected_failure() ? cudaErrorLaunchFailure : launch_token_logp(a, static_cast<cudaStream_t>(stream));
   }
   return e == cudaSuccess ? LS_OK : cuda_fail(e, "token log-prob launch");
 }
 
 ls_status ls_replay_fwd_prompt_only(ls_prefix_t h, int64_t R, const void* q, void* o, float* lse,
                                     void* stream) {
+  NvtxRange nvtx_range("ls_replay_fwd_prompt_only");
   ls_status st = check_handle(h);
   if (st != LS_OK) return st;
   if (R < 1) return LS_ERR_INVALID_ARGUMENT;
@@ -645,6 +687,7 @@ ls_status ls_replay_fwd_prompt_only(ls_prefix_t h, int64_t R, const void* q, voi
 ls_status ls_replay_bwd_prompt_only(ls_prefix_t h, int64_t R, const void* q, const void* o,
                                     const float* lse, const void* d_out, void* dq,
                                     void* workspace, size_t workspace_bytes, void* stream) {
+  NvtxRange nvtx_range("ls_replay_bwd_prompt_only");
   ls_status st = check_handle(h);
   if (st != LS_OK) return st;
   if (R < 1) return LS_ERR_INVALID_ARGUMENT;
@@ -655,6 +698,7 @@ ls_status ls_replay_bwd_prompt_only(ls_prefix_t h, int64_t R, const void* q, con
 
 ls_status ls_attn_merge(int32_t n, int64_t R, int32_t Hq, int32_t D, const void* const* o_parts,
                         const float* const* lse_parts, void* o, float* lse, void* stream) {
+  NvtxRange nvtx_range("ls_attn_merge");
   if (o_parts == nullptr || lse_parts == nullptr || o == nullptr || lse == nullptr)
     return LS_ERR_INVALID_ARGUMENT;
   if (n < 1 || R < 1 || Hq < 1 || D < 8) return LS_ERR_INVALID_ARGUMENT;
@@ -678,12 +722,13 @@ ls_status ls_attn_merge(int32_t n, int64_t R, int32_t Hq, int32_t D, const void*
   cudaError_t e;
   {
     LaunchTimer t(LS_KERNEL_MERGE, static_cast<cudaStream_t>(stream));
-    e = launch_attn_merge(a, static_cast<cudaStream_t>(stream));
+    e = injected_failure() ? cudaErrorLaunchFailure : launch_attn_merge(a, static_cast<cudaStream_t>(stream));
   }
   return e == cudaSuccess ? LS_OK : cuda_fail(e, "merge launch");
 }
 
 ls_status ls_sum_bf16(int32_t n, int64_t count, const void* const* parts, void* out, void* stream) {
+  NvtxRange nvtx_range("ls_sum_bf16");
   if (parts == nullptr || out == nullptr || n < 1 || count < 1) return LS_ERR_INVALID_ARGUMENT;
   if (n > kMaxParts || count % 8 != 0) return LS_ERR_UNSUPPORTED;
   SumArgs a{};
@@ -702,12 +747,13 @@ ls_status ls_sum_bf16(int32_t n, int64_t count, const void* const* parts, void* 
   cudaError_t e;
   {
     LaunchTimer t(LS_KERNEL_SUM, static_cast<cudaStream_t>(stream));
-    e = launch_sum_bf16(a, static_cast<cudaStream_t>(stream));
+    e = injected_failure() ? cudaErrorLaunchFailure : launch_sum_bf16(a, static_cast<cudaStream_t>(stream));
   }
   return e == cudaSuccess ? LS_OK : cuda_fail(e, "sum launch");
 }
 
 ls_status ls_bf16_to_f32(int64_t count, const void* in, float* out, void* stream) {
+  NvtxRange nvtx_range("ls_bf16_to_f32");
   if (in == nullptr || out == nullptr || count < 1) return LS_ERR_INVALID_ARGUMENT;
   if (count % 8 != 0) return LS_ERR_UNSUPPORTED;
   if (!aligned16(in) || !aligned16(out)) return LS_ERR_MISALIGNED;
@@ -717,12 +763,13 @@ ls_status ls_bf16_to_f32(int64_t count, const void* in, float* out, void* stream
   cudaError_t e;
   {
     LaunchTimer t(LS_KERNEL_CAST, static_cast<cudaStream_t>(stream));
-    e = launch_bf16_to_f32(in, out, static_cast<size_t>(count), static_cast<cudaStream_t>(stream));
+    e = injected_failure() ? cudaErrorLaunchFailure : launch_bf16_to_f32(in, out, static_cast<size_t>(count), static_cast<cudaStream_t>(stream));
   }
   return e == cudaSuccess ? LS_OK : cuda_fail(e, "bf16 -> fp32 launch");
 }
 
 ls_status ls_f32_to_bf16(int64_t count, const float* in, void* out, void* stream) {
+  NvtxRange nvtx_range("ls_f32_to_bf16");
   if (in == nullptr || out == nullptr || count < 1) return LS_ERR_INVALID_ARGUMENT;
   if (count % 8 != 0) return LS_ERR_UNSUPPORTED;
   if (!aligned16(in) || !aligned16(out)) return LS_ERR_MISALIGNED;
@@ -732,13 +779,14 @@ ls_status ls_f32_to_bf16(int64_t count, const float* in, void* out, void* stream
   cudaError_t e;
   {
     LaunchTimer t(LS_KERNEL_CAST, static_cast<cudaStream_t>(stream));
-    e = launch_f32_to_bf16(in, out, static_cast<size_t>(count), static_cast<cudaStream_t>(stream));
+    e = injected_failure() ? cudaErrorLaunchFailure : launch_f32_to_bf16(in, out, static_cast<size_t>(count), static_cast<cudaStream_t>(stream));
   }
   return e == cudaSuccess ? LS_OK : cuda_fail(e, "fp32 -> bf16 launch");
 }
 
 ls_status ls_prefix_grad_finalize(ls_prefix_t h, float scale, void* dk_out, void* dv_out,
                                   int out_is_fp32, int reset_acc, void* stream) {
+  NvtxRange nvtx_range("ls_prefix_grad_finalize");
   ls_status st = check_handle(h);
   if (st != LS_OK) return st;
   return finalize_impl(h, 0, h->shape.P, scale, dk_out, dv_out, out_is_fp32, reset_acc, stream);
@@ -747,6 +795,7 @@ ls_status ls_prefix_grad_finalize(ls_prefix_t h, float scale, void* dk_out, void
 ls_status ls_prefix_grad_finalize_rows(ls_prefix_t h, int64_t row0, int64_t nrows, float scale,
                                        void* dk_out, void* dv_out, int out_is_fp32,
                                        int reset_acc, void* stream) {
+  NvtxRange nvtx_range("ls_prefix_grad_finalize_rows");
   ls_status st = check_handle(h);
   if (st != LS_OK) return st;
   if (row0 < 0 || nrows < 1 || row0 > h->shape.P - nrows) return LS_ERR_INVALID_ARGUMENT;
@@ -754,13 +803,21 @@ ls_status ls_prefix_grad_finalize_rows(ls_prefix_t h, int64_t row0, int64_t nrow
 }
 
 ls_status ls_debug_wait_timeout(uint64_t limit_ns, void* stream) {
+  NvtxRange nvtx_range("ls_debug_wait_timeout");
   if (limit_ns == 0 || limit_ns > 10000000000ull) return LS_ERR_INVALID_ARGUMENT;
   uint32_t* status = nullptr;
   ls_status st = enter(nullptr, stream, &status);
   if (st != LS_OK) return st;
-  cudaError_t e = launch_wait_timeout(limit_ns, status, static_cast<cudaStream_t>(stream));
+  cudaError_t e = injected_failure() ? cudaErrorLaunchFailure : launch_wait_timeout(limit_ns, status, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? LS_OK : cuda_fail(e, "wait-timeout self test launch");
 }
+
+ls_status ls_debug_fail_launch(int64_t after) {
+  g_fail_countdown.store(after < 0 ? -1 : after);
+  return LS_OK;
+}
+
+int64_t ls_debug_fail_launch_pending(void) { return g_fail_countdown.load(); }
 
 ls_status ls_timing_enable(int enable) {
   std::lock_guard<std::mutex> lk(g_timing_mu);
@@ -801,6 +858,7 @@ ls_status ls_timing_read(double* total_ms, int64_t* launches, int n) {
 }
 
 ls_status ls_get_device_status(void* stream, uint32_t* bits) {
+  NvtxRange nvtx_range("ls_get_device_status");
   int dev = 0;
   ls_status st = current_device(&dev);
   if (st != LS_OK) return st;

@@ -163,5 +163,8 @@ void set_last_error(const char* msg);
 int enter_call(void* stream, uint32_t** status);
 // Records the CUDA message of a failed launch for ls_last_error(); returns LS_ERR_CUDA.
 int launch_failed(cudaError_t e, const char* what);
+// True when the launch attempt about to be made is the one ls_debug_fail_launch armed: the
+// caller then skips the launch and reports a launch failure.
+bool injected_failure();
 
 }  // namespace ls

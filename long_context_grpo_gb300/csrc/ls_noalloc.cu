@@ -108,7 +108,8 @@ extern "C" ls_status ls_grpo_loss_noalloc(int64_t R, int64_t V, int32_t G, const
   a.logp_out = logp_out;
   a.row_terms = scratch;
   a.status = status;
-  cudaError_t e = launch_grpo_loss(a, static_cast<cudaStream_t>(stream));
+  cudaError_t e = injected_failure() ? cudaErrorLaunchFailure
+                                     : launch_grpo_loss(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return static_cast<ls_status>(launch_failed(e, "grpo loss (no-allocation) launch"));
   return LS_OK;
 }
