@@ -42,6 +42,10 @@ namespace ls {
 namespace {
 
 constexpr int kThreads = 384;
+// Suspend-time hints (ns) of each role's mbarrier waits (0: the hardware's own limit; a
+// 20 ns hint measured slower here, see the forward kernel).
+constexpr uint32_t kHintDkdvProducer = 0u, kHintDkdvMma = 0u, kHintDkdvSoftmax = 0u;
+constexpr uint32_t kHintDqProducer = 0u, kHintDqMma = 0u, kHintDqSoftmax = 0u;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Column (within a 128-column TMEM region) of the packed bf16 A operand for k-step kk
@@ -226,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true, kv_pending = false;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
         const KvUnit w = make_kv_unit<kPacked, kNoSuffix>(u, sh, vl);
-        if (uc > 0) ok = mbar_wait(&bars[C::kBarKVEmpty], (uc - 1) & 1u, status, vabort);
+        if (uc > 0) ok = mbar_wait_hint<kHintDkdvProducer>(&bars[C::kBarKVEmpty], (uc - 1) & 1u, status, vabort);
         if (!ok) break;
         mbar_arrive_expect_tx(&bars[C::kBarKVFull], 2 * C::kTile);
         for (int b = 0; b < C::kBoxes; ++b) {
@@ -246,14 +250,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t sq = qit % C::kNQ, so = qit % C::kNO;
           if (qit >= static_cast<uint32_t>(C::kNQ))
-            ok = mbar_wait(&bars[C::kBarQEmpty + sq], ((qit / C::kNQ) - 1) & 1u, status, vabort);
+            ok = mbar_wait_hint<kHintDkdvProducer>(&bars[C::kBarQEmpty + sq], ((qit / C::kNQ) - 1) & 1u, status, vabort);
           if (!ok) break;
           mbar_arrive_expect_tx(&bars[C::kBarQFull + sq], tile_tx);
           for (int b = 0; b < C::kBoxes; ++b)
             tma_load_3d(smem + C::kOffQ + sq * C::kTile + b * 16384, &tm_q,
                         &bars[C::kBarQFull + sq], 64 * b, w.kv * sh.g, qrow);
           if (qit >= static_cast<uint32_t>(C::kNO))
-            ok = mbar_wait(&bars[C::kBarOEmpty + so], ((qit / C::kNO) - 1) & 1u, status, vabort);
+            ok = mbar_wait_hint<kHintDkdvProducer>(&bars[C::kBarOEmpty + so], ((qit / C::kNO) - 1) & 1u, status, vabort);
           if (!ok) break;
           mbar_arrive_expect_tx(&bars[C::kBarOFull + so], tile_tx);
           for (int b = 0; b < C::kBoxes; ++b)
@@ -288,8 +292,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // previous S out of TMEM
       auto issue_s = [&](uint32_t it) -> bool {
         const uint32_t sq = it % C::kNQ;
-        if (!mbar_wait(&bars[C::kBarQFull + sq], (it / C::kNQ) & 1u, status, vabort)) return false;
-        if (n_s > 0 && !mbar_wait(&bars[C::kBarSFree], (n_s - 1) & 1u, status, vabort))
+        if (!mbar_wait_hint<kHintDkdvMma>(&bars[C::kBarQFull + sq], (it / C::kNQ) & 1u, status, vabort)) return false;
+        if (n_s > 0 && !mbar_wait_hint<kHintDkdvMma>(&bars[C::kBarSFree], (n_s - 1) & 1u, status, vabort))
           return false;
         tc_fence_after();
         const uint64_t q = dQk + static_cast<uint64_t>((sq * C::kTile) >> 4);
@@ -304,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto issue_dp = [&](uint32_t it) -> bool {
         const uint32_t so = it % C::kNO;
-        if (!mbar_wait(&bars[C::kBarOFull + so], (it / C::kNO) & 1u, status, vabort)) return false;
+        if (!mbar_wait_hint<kHintDkdvMma>(&bars[C::kBarOFull + so], (it / C::kNO) & 1u, status, vabort)) return false;
         tc_fence_after();
         const uint64_t o_ = dOk + static_cast<uint64_t>((so * C::kTile) >> 4);
 #pragma unroll
@@ -330,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
         const KvUnit w = make_kv_unit<kPacked, kNoSuffix>(u, sh, vl);
-        ok = mbar_wait(&bars[C::kBarKVFull], uc & 1u, status, vabort);
+        ok = mbar_wait_hint<kHintDkdvMma>(&bars[C::kBarKVFull], uc & 1u, status, vabort);
         if (!ok) break;
         tc_fence_after();
         ok = issue_s(qit) && issue_dp(qit);
@@ -341,11 +345,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = issue_s(it + 1);
             if (!ok) break;
           }
-          ok = mbar_wait(&bars[C::kBarPDSFull], n_pds & 1u, status, vabort);
+          ok = mbar_wait_hint<kHintDkdvMma>(&bars[C::kBarPDSFull], n_pds & 1u, status, vabort);
           if (!ok) break;
           ++n_pds;
           if (li == 0 && uc > 0) {
-            ok = mbar_wait(&bars[C::kBarAccFree], (uc - 1) & 1u, status, vabort);
+            ok = mbar_wait_hint<kHintDkdvMma>(&bars[C::kBarAccFree], (uc - 1) & 1u, status, vabort);
             if (!ok) break;
           }
           tc_fence_after();
@@ -378,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float* rs = rowstats + (static_cast<int64_t>(w.kv) * n_qt + w.f0 + li) * 256;
         const float4* lse4 = reinterpret_cast<const float4*>(rs) + wg * 16;   // rows 64 wg ..
         const float4* dlt4 = reinterpret_cast<const float4*>(rs + 128) + wg * 16;
-        ok = mbar_wait(&bars[C::kBarSFull], n_tiles & 1u, status, vabort);
+        ok = mbar_wait_hint<kHintDkdvSoftmax>(&bars[C::kBarSFull], n_tiles & 1u, status, vabort);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
@@ -431,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         // ---- dS^T from dP^T; packed P^T / dS^T replace the fp32 dP^T chunk just read
-        ok = mbar_wait(&bars[C::kBarDPFull], (n_tiles & 1u), status, vabort);
+        ok = mbar_wait_hint<kHintDkdvSoftmax>(&bars[C::kBarDPFull], (n_tiles & 1u), status, vabort);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
@@ -469,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       qit += w.n;
       // epilogue: warpgroup 0 owns dV, warpgroup 1 owns dK
-      ok = mbar_wait(&bars[C::kBarAccDone], uc & 1u, status, vabort);
+      ok = mbar_wait_hint<kHintDkdvSoftmax>(&bars[C::kBarAccDone], uc & 1u, status, vabort);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -677,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
         const QUnit w = pick_q_unit<kPacked, kNoSuffix>(u, sh, n_qt, vl);
-        if (uc > 0) ok = mbar_wait(&bars[C::kBarQEmpty], (uc - 1) & 1u, status, vabort);
+        if (uc > 0) ok = mbar_wait_hint<kHintDqProducer>(&bars[C::kBarQEmpty], (uc - 1) & 1u, status, vabort);
         if (!ok) break;
         mbar_arrive_expect_tx(&bars[C::kBarQFull],
                               static_cast<uint32_t>(2 * C::kBoxes * 128 * sh.g * sh.qt));
@@ -692,14 +696,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int key0 = pre ? 128 * j : (kPacked ? w.base : 0) + 128 * (j - w.n_pt);
           const uint32_t sk = kit % C::kNK, sv = kit % C::kNV;
           if (kit >= static_cast<uint32_t>(C::kNK))
-            ok = mbar_wait(&bars[C::kBarKEmpty + sk], ((kit / C::kNK) - 1) & 1u, status, vabort);
+            ok = mbar_wait_hint<kHintDqProducer>(&bars[C::kBarKEmpty + sk], ((kit / C::kNK) - 1) & 1u, status, vabort);
           if (!ok) break;
           mbar_arrive_expect_tx(&bars[C::kBarKFull + sk], C::kTile);
           for (int b = 0; b < C::kBoxes; ++b)
             tma_load_3d(smem + C::kOffK + sk * C::kTile + b * 16384, pre ? &tm_kp : &tm_ks,
                         &bars[C::kBarKFull + sk], 64 * b, w.kv, key0);
           if (kit >= static_cast<uint32_t>(C::kNV))
-            ok = mbar_wait(&bars[C::kBarVEmpty + sv], ((kit / C::kNV) - 1) & 1u, status, vabort);
+            ok = mbar_wait_hint<kHintDqProducer>(&bars[C::kBarVEmpty + sv], ((kit / C::kNV) - 1) & 1u, status, vabort);
           if (!ok) break;
           mbar_arrive_expect_tx(&bars[C::kBarVFull + sv], C::kTile);
           for (int b = 0; b < C::kBoxes; ++b)
@@ -730,8 +734,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the previous S out of TMEM
       auto issue_s = [&](uint32_t it) -> bool {
         const uint32_t sk = it % C::kNK;
-        if (!mbar_wait(&bars[C::kBarKFull + sk], (it / C::kNK) & 1u, status, vabort)) return false;
-        if (n_s > 0 && !mbar_wait(&bars[C::kBarSFree], (n_s - 1) & 1u, status, vabort))
+        if (!mbar_wait_hint<kHintDqMma>(&bars[C::kBarKFull + sk], (it / C::kNK) & 1u, status, vabort)) return false;
+        if (n_s > 0 && !mbar_wait_hint<kHintDqMma>(&bars[C::kBarSFree], (n_s - 1) & 1u, status, vabort))
           return false;
         tc_fence_after();
         const uint64_t k = dKk + static_cast<uint64_t>((sk * C::kTile) >> 4);
@@ -746,7 +750,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto issue_dp = [&](uint32_t it) -> bool {
         const uint32_t sv = it % C::kNV;
-        if (!mbar_wait(&bars[C::kBarVFull + sv], (it / C::kNV) & 1u, status, vabort)) return false;
+        if (!mbar_wait_hint<kHintDqMma>(&bars[C::kBarVFull + sv], (it / C::kNV) & 1u, status, vabort)) return false;
         tc_fence_after();
         const uint64_t v = dVk + static_cast<uint64_t>((sv * C::kTile) >> 4);
 #pragma unroll
@@ -771,7 +775,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
         const QUnit w = pick_q_unit<kPacked, kNoSuffix>(u, sh, n_qt, vl);
-        ok = mbar_wait(&bars[C::kBarQTmem], uc & 1u, status, vabort);
+        ok = mbar_wait_hint<kHintDqMma>(&bars[C::kBarQTmem], uc & 1u, status, vabort);
         if (!ok) break;
         tc_fence_after();
         ok = issue_s(kit) && issue_dp(kit);
@@ -782,11 +786,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = issue_s(it + 1);
             if (!ok) break;
           }
-          ok = mbar_wait(&bars[C::kBarDSFull], n_ds & 1u, status, vabort);
+          ok = mbar_wait_hint<kHintDqMma>(&bars[C::kBarDSFull], n_ds & 1u, status, vabort);
           if (!ok) break;
           ++n_ds;
           if (j == 0 && uc > 0) {
-            ok = mbar_wait(&bars[C::kBarDQFree], (uc - 1) & 1u, status, vabort);
+            ok = mbar_wait_hint<kHintDqMma>(&bars[C::kBarDQFree], (uc - 1) & 1u, status, vabort);
             if (!ok) break;
           }
           tc_fence_after();
@@ -823,7 +827,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // stage this unit's Q (warpgroup 0) or dO (warpgroup 1) row into TMEM; the previous
       // unit's MMAs have all completed (its dQ-done barrier was waited on)
-      ok = mbar_wait(&bars[C::kBarQFull], uc & 1u, status, vabort);
+      ok = mbar_wait_hint<kHintDqSoftmax>(&bars[C::kBarQFull], uc & 1u, status, vabort);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       {
@@ -848,7 +852,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&bars[C::kBarQEmpty]);
       }
       for (int j = 0; j < w.n; ++j, ++n_steps) {
-        ok = mbar_wait(&bars[C::kBarSFull], n_steps & 1u, status, vabort);
+        ok = mbar_wait_hint<kHintDqSoftmax>(&bars[C::kBarSFull], n_steps & 1u, status, vabort);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
@@ -891,16 +895,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (wg * 64 + i >= lim) p[i] = 0.0f;
         }
         // ---- dS from dP; packed dS replaces the fp32 dP chunk just read
-        ok = mbar_wait(&bars[C::kBarDPFull], n_steps & 1u, status, vabort);
+        ok = mbar_wait_hint<kHintDqSoftmax>(&bars[C::kBarDPFull], n_steps & 1u, status, vabort);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
+        // both dP chunks are read with one wait (a single TMEM round trip)
+        uint32_t dva[2][32];
+        tmem_ld32(lane_base + C::kColDP + wg * 64, dva[0]);
+        tmem_ld32(lane_base + C::kColDP + wg * 64 + 32, dva[1]);
+        tmem_ld_wait();
 #pragma unroll
         for (int ch = 0; ch < 2; ++ch) {
-          uint32_t dv[32];
+          const uint32_t* dv = dva[ch];
           const uint32_t col = C::kColDP + wg * 64 + ch * 32;
-          tmem_ld32(lane_base + col, dv);
-          tmem_ld_wait();
           uint32_t dw[16];
           const uint64_t dlt2 = f2_pack(dlt, dlt);
 #pragma unroll
@@ -920,7 +927,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // epilogue: dQ * s -> bf16; warpgroup 0 stores columns [0, D/2), warpgroup 1 the rest
-      ok = mbar_wait(&bars[C::kBarDQDone], uc & 1u, status, vabort);
+      ok = mbar_wait_hint<kHintDqSoftmax>(&bars[C::kBarDQDone], uc & 1u, status, vabort);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();

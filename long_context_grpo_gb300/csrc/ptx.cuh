@@ -104,6 +104,55 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   }
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete yet is suspended
+// at most kHintNs nanoseconds before it polls again (0: the hardware's own limit).
+template <uint32_t kHintNs>
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity) {
+  if constexpr (kHintNs == 0u) {
+    return mbar_try_wait(bar, parity);
+  } else {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "n"(kHintNs)
+        : "memory");
+    return ok != 0u;
+  }
+}
+
+// mbar_wait (bounded, with or without the abort flag) polling with a suspend-time hint.
+template <uint32_t kHintNs>
+__device__ __forceinline__ bool mbar_wait_hint(uint64_t* bar, uint32_t parity, uint32_t* status) {
+  if (mbar_try_wait_hint<kHintNs>(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait_hint<kHintNs>(bar, parity)) return true;
+    if ((i & 63u) == 0u && globaltimer_ns() - t0 > LS_WAIT_LIMIT_NS) {
+      set_device_status(status, DEV_WAIT_TIMEOUT);
+      return false;
+    }
+  }
+}
+template <uint32_t kHintNs>
+__device__ __forceinline__ bool mbar_wait_hint(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                               volatile int* abort) {
+  if (mbar_try_wait_hint<kHintNs>(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait_hint<kHintNs>(bar, parity)) return true;
+    if ((i & 63u) == 0u) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > LS_WAIT_LIMIT_NS) {
+        set_device_status(status, DEV_WAIT_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
 // Same wait with a caller-chosen limit (used on teardown after an abort).
 __device__ __forceinline__ bool mbar_wait_ns(uint64_t* bar, uint32_t parity, uint64_t limit) {
   const uint64_t t0 = globaltimer_ns();

@@ -18,20 +18,25 @@ def test_pairs_counts_visible_query_key_pairs():
 
 
 def test_traffic_is_scaled_by_work_units_and_gated_by_the_source_hash(tmp_path, monkeypatch):
+    """The dK/dV traffic record scales by 128-key work units, and only while the recorded
+    hash equals the kernel source's (a stale record gives no number)."""
+    import hashlib
     from long_context_grpo_gb300 import workloads as wl
     w = wl.WORKLOADS["p2m"]
-    t = bench.load_traffic(w, [128, 256])
     rec = json.load(open(os.path.join(bench.ROOT, "profiles", "ncu_traffic.json")))["bwd_dkdv"]
-    units = [w.Hkv * (w.P // 128 + 1), w.Hkv * (w.P // 128 + 2)]
-    assert t == pytest.approx(rec["dram_bytes_per_unit"] * sum(units) / 2)
-    # a record whose hash no longer matches the kernel source gives no number
-    fake = dict(rec, kernel_source_sha256_16="0" * 16)
-    os.makedirs(tmp_path / "profiles")
-    json.dump({"bwd_dkdv": fake}, open(tmp_path / "profiles" / "ncu_traffic.json", "w"))
+    src_bytes = open(os.path.join(bench.ROOT, rec["kernel_source"]), "rb").read()
     src = tmp_path / rec["kernel_source"]
     os.makedirs(src.parent, exist_ok=True)
-    src.write_bytes(open(os.path.join(bench.ROOT, rec["kernel_source"]), "rb").read())
+    src.write_bytes(src_bytes)
+    os.makedirs(tmp_path / "profiles")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    units = [w.Hkv * (w.P // 128 + 1), w.Hkv * (w.P // 128 + 2)]
+    fresh = dict(rec, dram_bytes_per_unit=300000,
+                 kernel_source_sha256_16=hashlib.sha256(src_bytes).hexdigest()[:16])
+    json.dump({"bwd_dkdv": fresh}, open(tmp_path / "profiles" / "ncu_traffic.json", "w"))
+    assert bench.load_traffic(w, [128, 256]) == pytest.approx(300000 * sum(units) / 2)
+    stale = dict(fresh, kernel_source_sha256_16="0" * 16)
+    json.dump({"bwd_dkdv": stale}, open(tmp_path / "profiles" / "ncu_traffic.json", "w"))
     assert bench.load_traffic(w, [128]) is None
 
 
