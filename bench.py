@@ -907,6 +907,52 @@ def run_ours(args, w):
         dist.destroy_process_group()
 
 
+def run_loss_only(args):
+    """The GRPO loss and token log-prob kernels alone on one synthetic response of R rows of
+    the workload's vocabulary (the shape of the committed loss capture): one untimed log-prob
+    pass, `warmup` untimed loss calls, then `steps` timed loss calls and `steps` timed
+    log-prob calls with CUDA events.  Prints one JSON line (a kernel measurement, not the
+    group-step line)."""
+    import torch
+    import long_context_grpo_gb300 as ls
+    from long_context_grpo_gb300 import workloads as wl
+    w = wl.WORKLOADS[args.workload]
+    torch.cuda.set_device(0)
+    R = args.loss_rows
+    logits, ids, noise = wl.response_loss_inputs(w, 0, R, args.seed, "cuda")
+    old = ls.token_logp(logits, ids) + noise
+    loss = torch.zeros(1, dtype=torch.float64, device="cuda")
+    dl = torch.empty_like(logits)
+    mask = torch.empty((R,), dtype=torch.uint8, device="cuda")
+    lp = torch.empty((R,), dtype=torch.float32, device="cuda")
+    ws = torch.empty(ls.grpo_loss_workspace_bytes(R), dtype=torch.uint8, device="cuda")
+    for _ in range(args.warmup):
+        ls.grpo_loss(logits, ids, old, 0.7, w.eps, w.G, loss, dlogits=dl, clip_mask=mask,
+                     logp_out=lp, workspace=ws)
+    torch.cuda.synchronize()
+    e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    e[0].record()
+    for _ in range(args.steps):
+        ls.grpo_loss(logits, ids, old, 0.7, w.eps, w.G, loss, dlogits=dl, clip_mask=mask,
+                     logp_out=lp, workspace=ws)
+    e[1].record()
+    for _ in range(args.steps):
+        ls.token_logp(logits, ids, logp_out=lp)
+    e[2].record()
+    torch.cuda.synchronize()
+    if ls.device_status() != (0, 0):
+        raise RuntimeError("device status set")
+    peaks, src = load_peaks()
+    ms_l = e[0].elapsed_time(e[1]) / args.steps
+    ms_s = e[1].elapsed_time(e[2]) / args.steps
+    gb_l = R * (4 * w.V + 12) / (ms_l / 1e3) / 1e9
+    gb_s = R * (2 * w.V + 8) / (ms_s / 1e3) / 1e9
+    print(json.dumps({"kernel": "grpo_loss + token_logp", "rows": R, "V": w.V,
+                      "loss_ms": ms_l, "loss_gbs": gb_l, "loss_frac_hbm": gb_l / peaks["hbm_gbs"],
+                      "logp_ms": ms_s, "logp_gbs": gb_s, "logp_frac_hbm": gb_s / peaks["hbm_gbs"],
+                      "peak_gbs": peaks["hbm_gbs"], "peak_source": src + " HBM copy"}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -924,6 +970,9 @@ def main():
     ap.add_argument("--no-packed", action="store_true")
     ap.add_argument("--cp-shards", type=int, default=8,
                     help="prompt shards of the context-parallel measurement (0: skip it)")
+    ap.add_argument("--loss-only", action="store_true",
+                    help="time only the loss and log-prob kernels on --loss-rows rows")
+    ap.add_argument("--loss-rows", type=int, default=4096)
     ap.add_argument("--configs", default="tiny,p32k,p262k,p1m",
                     help="other workloads whose group step is timed too ('' : none)")
     ap.add_argument("--config-steps", type=int, default=2)
@@ -938,6 +987,8 @@ def main():
         if int(os.environ.get("RANK", "0")) != 0:
             return
         run_reference(args, w)
+    elif args.loss_only:
+        run_loss_only(args)
     else:
         run_ours(args, w)
 
