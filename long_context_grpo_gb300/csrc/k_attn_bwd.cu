@@ -226,10 +226,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_vs);
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_do);
-      uint32_t qit = 0, uc = 0;
+      uint32_t qit = 0, uc = 0, q_sent = 0;
       bool ok = true, kv_pending = false;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
         const KvUnit w = make_kv_unit<kPacked, kNoSuffix>(u, sh, vl);
+        kv_pending = false;
         if (uc > 0) ok = mbar_wait_hint<kHintDkdvProducer>(&bars[C::kBarKVEmpty], (uc - 1) & 1u, status, vabort);
         if (!ok) break;
         mbar_arrive_expect_tx(&bars[C::kBarKVFull], 2 * C::kTile);
@@ -256,6 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int b = 0; b < C::kBoxes; ++b)
             tma_load_3d(smem + C::kOffQ + sq * C::kTile + b * 16384, &tm_q,
                         &bars[C::kBarQFull + sq], 64 * b, w.kv * sh.g, qrow);
+          ++q_sent;
           if (qit >= static_cast<uint32_t>(C::kNO))
             ok = mbar_wait_hint<kHintDkdvProducer>(&bars[C::kBarOEmpty + so], ((qit / C::kNO) - 1) & 1u, status, vabort);
           if (!ok) break;
@@ -268,7 +270,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) {
         *vabort = 1;
         // drain this thread's own copies still in flight (the last issues of each ring)
-        for (uint32_t it = qit > static_cast<uint32_t>(C::kNQ) ? qit - C::kNQ : 0u; it < qit; ++it)
+        // (a Q tile may have been sent in the iteration whose O wait gave up)
+        for (uint32_t it = q_sent > static_cast<uint32_t>(C::kNQ) ? q_sent - C::kNQ : 0u; it < q_sent; ++it)
           mbar_wait_ns(&bars[C::kBarQFull + it % C::kNQ], (it / C::kNQ) & 1u, 200000000ull);
         for (uint32_t it = qit > static_cast<uint32_t>(C::kNO) ? qit - C::kNO : 0u; it < qit; ++it)
           mbar_wait_ns(&bars[C::kBarOFull + it % C::kNO], (it / C::kNO) & 1u, 200000000ull);
@@ -677,12 +680,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_vs);
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_do);
-      uint32_t kit = 0, uc = 0;
-      bool ok = true;
+      uint32_t kit = 0, uc = 0, k_sent = 0;
+      bool ok = true, q_sent = false;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
         const QUnit w = pick_q_unit<kPacked, kNoSuffix>(u, sh, n_qt, vl);
+        q_sent = false;
         if (uc > 0) ok = mbar_wait_hint<kHintDqProducer>(&bars[C::kBarQEmpty], (uc - 1) & 1u, status, vabort);
         if (!ok) break;
+        q_sent = true;
         mbar_arrive_expect_tx(&bars[C::kBarQFull],
                               static_cast<uint32_t>(2 * C::kBoxes * 128 * sh.g * sh.qt));
         for (int b = 0; b < C::kBoxes; ++b) {
@@ -702,6 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int b = 0; b < C::kBoxes; ++b)
             tma_load_3d(smem + C::kOffK + sk * C::kTile + b * 16384, pre ? &tm_kp : &tm_ks,
                         &bars[C::kBarKFull + sk], 64 * b, w.kv, key0);
+          ++k_sent;
           if (kit >= static_cast<uint32_t>(C::kNV))
             ok = mbar_wait_hint<kHintDqProducer>(&bars[C::kBarVEmpty + sv], ((kit / C::kNV) - 1) & 1u, status, vabort);
           if (!ok) break;
@@ -713,11 +719,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) {
         *vabort = 1;
-        for (uint32_t it = kit > static_cast<uint32_t>(C::kNK) ? kit - C::kNK : 0u; it < kit; ++it)
+        // drain this thread's own copies still in flight (a K tile may have been sent in the
+        // iteration whose V wait gave up)
+        for (uint32_t it = k_sent > static_cast<uint32_t>(C::kNK) ? k_sent - C::kNK : 0u; it < k_sent; ++it)
           mbar_wait_ns(&bars[C::kBarKFull + it % C::kNK], (it / C::kNK) & 1u, 200000000ull);
         for (uint32_t it = kit > static_cast<uint32_t>(C::kNV) ? kit - C::kNV : 0u; it < kit; ++it)
           mbar_wait_ns(&bars[C::kBarVFull + it % C::kNV], (it / C::kNV) & 1u, 200000000ull);
-        mbar_wait_ns(&bars[C::kBarQFull], (uc) & 1u, 200000000ull);
+        if (q_sent) mbar_wait_ns(&bars[C::kBarQFull], uc & 1u, 200000000ull);
       }
     }
   } else if (warp == 1) {
