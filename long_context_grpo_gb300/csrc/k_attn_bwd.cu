@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    {
       constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t kIdAcc = idesc_bf16(128, D, false, true);
       const uint64_t dK0 = smem_desc(smem_u32(smem + C::kOffK), 16, 1024);
@@ -303,9 +303,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t o = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-          mma_bf16_ss(tmem + C::kColS, dK0 + o, q + o, kIdS, kk > 0 ? 1u : 0u);
+          mma_bf16_ss_w(tmem + C::kColS, dK0 + o, q + o, kIdS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&bars[C::kBarSFull]);
+        mma_commit_w(&bars[C::kBarSFull]);
         ++n_s;
         return true;
       };
@@ -317,9 +317,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t o = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-          mma_bf16_ss(tmem + C::kColDP, dV0 + o, o_ + o, kIdS, kk > 0 ? 1u : 0u);
+          mma_bf16_ss_w(tmem + C::kColDP, dV0 + o, o_ + o, kIdS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&bars[C::kBarDPFull]);
+        mma_commit_w(&bars[C::kBarDPFull]);
         return true;
       };
       auto issue_acc = [&](uint32_t it, bool acc) {
@@ -329,11 +329,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t ko = static_cast<uint64_t>((kk * 2048) >> 4);
           const uint32_t pc = tmem + C::kColDP + packed_col(kk);
-          mma_bf16_ts(tmem + C::kColDV, pc, o + ko, kIdAcc, (acc || kk > 0) ? 1u : 0u);
-          mma_bf16_ts(tmem + C::kColDK, pc + 16u, q + ko, kIdAcc, (acc || kk > 0) ? 1u : 0u);
+          mma_bf16_ts_w(tmem + C::kColDV, pc, o + ko, kIdAcc, (acc || kk > 0) ? 1u : 0u);
+          mma_bf16_ts_w(tmem + C::kColDK, pc + 16u, q + ko, kIdAcc, (acc || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&bars[C::kBarQEmpty + it % C::kNQ]);
-        mma_commit(&bars[C::kBarOEmpty + it % C::kNO]);
+        mma_commit_w(&bars[C::kBarQEmpty + it % C::kNQ]);
+        mma_commit_w(&bars[C::kBarOEmpty + it % C::kNO]);
       };
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
         const KvUnit w = make_kv_unit<kPacked, kNoSuffix>(u, sh, vl);
@@ -361,11 +361,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         qit += w.n;
-        mma_commit(&bars[C::kBarAccDone]);
-        if (u + static_cast<int>(gridDim.x) < n_units) mma_commit(&bars[C::kBarKVEmpty]);
+        mma_commit_w(&bars[C::kBarAccDone]);
+        if (u + static_cast<int>(gridDim.x) < n_units) mma_commit_w(&bars[C::kBarKVEmpty]);
       }
       if (!ok) *vabort = 1;
-      mma_commit(&bars[C::kBarDrain]);
+      mma_commit_w(&bars[C::kBarDrain]);
       mbar_wait_ns(&bars[C::kBarDrain], 0u, ok ? LS_WAIT_LIMIT_NS : 200000000ull);
     }
   } else if (warp >= 4) {
@@ -730,7 +730,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    {
       constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t kIdQ = idesc_bf16(128, D, false, true);
       const uint64_t dKk = smem_desc(smem_u32(smem + C::kOffK), 16, 1024);      // K-major
@@ -750,9 +750,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t o = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-          mma_bf16_ts(tmem + C::kColS, tmem + C::kColQ + kk * 8, k + o, kIdS, kk > 0 ? 1u : 0u);
+          mma_bf16_ts_w(tmem + C::kColS, tmem + C::kColQ + kk * 8, k + o, kIdS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&bars[C::kBarSFull]);
+        mma_commit_w(&bars[C::kBarSFull]);
         ++n_s;
         return true;
       };
@@ -764,11 +764,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t o = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-          mma_bf16_ts(tmem + C::kColDP, tmem + C::kColDO + kk * 8, v + o, kIdS,
+          mma_bf16_ts_w(tmem + C::kColDP, tmem + C::kColDO + kk * 8, v + o, kIdS,
                       kk > 0 ? 1u : 0u);
         }
-        mma_commit(&bars[C::kBarDPFull]);
-        mma_commit(&bars[C::kBarVEmpty + sv]);   // V is read by dP only
+        mma_commit_w(&bars[C::kBarDPFull]);
+        mma_commit_w(&bars[C::kBarVEmpty + sv]);   // V is read by dP only
         return true;
       };
       auto issue_dq = [&](uint32_t it, bool acc) {
@@ -776,10 +776,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t k = dKm + static_cast<uint64_t>((sk * C::kTile) >> 4);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ts(tmem + C::kColDQ, tmem + C::kColDP + packed_col(kk),
+          mma_bf16_ts_w(tmem + C::kColDQ, tmem + C::kColDP + packed_col(kk),
                       k + static_cast<uint64_t>((kk * 2048) >> 4), kIdQ,
                       (acc || kk > 0) ? 1u : 0u);
-        mma_commit(&bars[C::kBarKEmpty + sk]);
+        mma_commit_w(&bars[C::kBarKEmpty + sk]);
       };
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
         const QUnit w = pick_q_unit<kPacked, kNoSuffix>(u, sh, n_qt, vl);
@@ -807,10 +807,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         kit += w.n;
-        mma_commit(&bars[C::kBarDQDone]);
+        mma_commit_w(&bars[C::kBarDQDone]);
       }
       if (!ok) *vabort = 1;
-      mma_commit(&bars[C::kBarDrain]);
+      mma_commit_w(&bars[C::kBarDrain]);
       mbar_wait_ns(&bars[C::kBarDrain], 0u, ok ? LS_WAIT_LIMIT_NS : 200000000ull);
     }
   } else if (warp >= 4) {

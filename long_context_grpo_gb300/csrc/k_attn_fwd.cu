@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    {
       constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t kIdPV = idesc_bf16(128, D, false, true);
       const uint32_t sQ = smem_u32(smem + C::kOffQ);
@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t off = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-          mma_bf16_ss(d, qa + off, ka + off, kIdS, kk > 0 ? 1u : 0u);
+          mma_bf16_ss_w(d, qa + off, ka + off, kIdS, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int q, uint32_t vstage, bool acc) {
@@ -274,71 +274,71 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d = tmem + C::col_o(q), a = tmem + C::col_s(q);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ts(d, a + kk * 8, va + static_cast<uint64_t>((kk * 2048) >> 4), kIdPV,
+          mma_bf16_ts_w(d, a + kk * 8, va + static_cast<uint64_t>((kk * 2048) >> 4), kIdPV,
                       (acc || kk > 0) ? 1u : 0u);
       };
 
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
         const Unit w = pick_unit<kPacked, kNoSuffix>(u, sh, n_pairs, vl);
         const int nq = w.has1 ? 2 : 1;
-        ok = mbar_wait_hint<kHintFwdMma>(&bars[C::kBarQFull], uc & 1u, status, vabort);
+        ok = mbar_wait_warp<kHintFwdMma>(&bars[C::kBarQFull], uc & 1u, status, vabort);
         if (!ok) break;
         tc_fence_after();
         // S_q(0)
         uint32_t ks = kit % C::kNK;
-        ok = mbar_wait_hint<kHintFwdMma>(&bars[C::kBarKFull + ks], (kit / C::kNK) & 1u, status, vabort);
+        ok = mbar_wait_warp<kHintFwdMma>(&bars[C::kBarKFull + ks], (kit / C::kNK) & 1u, status, vabort);
         if (!ok) break;
         tc_fence_after();
         for (int q = 0; q < nq; ++q) {
           issue_s(q, ks);
-          mma_commit(&bars[C::kBarSFull + q]);
+          mma_commit_w(&bars[C::kBarSFull + q]);
         }
-        mma_commit(&bars[C::kBarKEmpty + ks]);
+        mma_commit_w(&bars[C::kBarKEmpty + ks]);
         ++kit;
         for (int j = 0; j < w.n_kt && ok; ++j) {
           const uint32_t vs = vit % C::kNV;
-          ok = mbar_wait_hint<kHintFwdMma>(&bars[C::kBarVFull + vs], (vit / C::kNV) & 1u, status, vabort);
+          ok = mbar_wait_warp<kHintFwdMma>(&bars[C::kBarVFull + vs], (vit / C::kNV) & 1u, status, vabort);
           if (!ok) break;
           const bool more = (j + 1) < w.n_kt;
           uint32_t ks_next = kit % C::kNK;
           for (int q = 0; q < nq && ok; ++q) {
-            ok = mbar_wait_hint<kHintFwdMma>(&bars[C::kBarPFull + q], (pph >> q) & 1u, status, vabort);
+            ok = mbar_wait_warp<kHintFwdMma>(&bars[C::kBarPFull + q], (pph >> q) & 1u, status, vabort);
             if (!ok) break;
             pph ^= 1u << q;
             const uint32_t uqq = q ? uq1 : uq0;
             if (j == 0 && uqq > 0) {
-              ok = mbar_wait_hint<kHintFwdMma>(&bars[C::kBarOFree + q], (uqq - 1) & 1u, status, vabort);
+              ok = mbar_wait_warp<kHintFwdMma>(&bars[C::kBarOFree + q], (uqq - 1) & 1u, status, vabort);
               if (!ok) break;
             }
             tc_fence_after();
             issue_pv(q, vs, j > 0);
-            if (!more) mma_commit(&bars[C::kBarODone + q]);
+            if (!more) mma_commit_w(&bars[C::kBarODone + q]);
             if (more) {
               if (q == 0) {
-                ok = mbar_wait_hint<kHintFwdMma>(&bars[C::kBarKFull + ks_next], (kit / C::kNK) & 1u, status, vabort);
+                ok = mbar_wait_warp<kHintFwdMma>(&bars[C::kBarKFull + ks_next], (kit / C::kNK) & 1u, status, vabort);
                 if (!ok) break;
                 tc_fence_after();
               }
               issue_s(q, ks_next);
-              mma_commit(&bars[C::kBarSFull + q]);
+              mma_commit_w(&bars[C::kBarSFull + q]);
             }
           }
           if (!ok) break;
           if (more) {
-            mma_commit(&bars[C::kBarKEmpty + ks_next]);
+            mma_commit_w(&bars[C::kBarKEmpty + ks_next]);
             ++kit;
           }
-          mma_commit(&bars[C::kBarVEmpty + vs]);
+          mma_commit_w(&bars[C::kBarVEmpty + vs]);
           ++vit;
         }
         if (!ok) break;
         ++uq0;
         if (nq > 1) ++uq1;
-        if (u + static_cast<int>(gridDim.x) < n_units) mma_commit(&bars[C::kBarQEmpty]);
+        if (u + static_cast<int>(gridDim.x) < n_units) mma_commit_w(&bars[C::kBarQEmpty]);
       }
       if (!ok) *vabort = 1;
       // drain: every MMA (and the arrivals committed behind it) has landed before exit
-      mma_commit(&bars[C::kBarDrain]);
+      mma_commit_w(&bars[C::kBarDrain]);
       mbar_wait_ns(&bars[C::kBarDrain], 0u, ok ? LS_WAIT_LIMIT_NS : 200000000ull);
     }
   } else if (warp >= 4) {

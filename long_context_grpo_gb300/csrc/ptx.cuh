@@ -371,6 +371,54 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
       : "memory");
 }
 
+// ---------------------------------------------------------------------------------------
+// Warp-issued forms: the calling warp is converged (all 32 lanes execute the call) and one
+// lane, picked by elect.sync, issues the instruction under a predicate.  Keeping the MMA
+// warp converged -- its waits run in every lane, with no lane-0 branch around them --
+// keeps the tensor pipe fed: measured on GB300, groups of eight 128x128x16 MMAs separated by
+// an mbarrier wait and a commit ran at 83 clocks per MMA from a lone lane 0 and at the full
+// 64 from a converged warp.
+// ---------------------------------------------------------------------------------------
+// The bounded wait of a converged warp with the outcome voted warp-uniform.  (Lanes of a
+// converged warp that poll the same barrier see the same result anyway; the vote is a timing
+// choice, measured per kernel: it helps the forward's issuer and slows the backward's.)
+template <uint32_t kHintNs>
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                               volatile int* abort) {
+  return __all_sync(0xffffffffu, mbar_wait_hint<kHintNs>(bar, parity, status, abort));
+}
+
+__device__ __forceinline__ void mma_bf16_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 r;\n\t"
+      "elect.sync r|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 r;\n\t"
+      "elect.sync r|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_w(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\t"
+      "elect.sync r|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
 // TMEM -> registers: this warp's 32 lanes, 32 consecutive 32-bit columns from `taddr`.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
