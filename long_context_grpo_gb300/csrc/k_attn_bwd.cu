@@ -74,8 +74,9 @@ struct DkdvCfg {
   static constexpr int kBarSFull = kBarOEmpty + kNO;
   static constexpr int kBarSFree = kBarSFull + 1;
   static constexpr int kBarDPFull = kBarSFree + 1;
+  // P/dS written, per 32-column chunk of each warpgroup (chunk c: k-steps with bit 1 = c)
   static constexpr int kBarPDSFull = kBarDPFull + 1;
-  static constexpr int kBarAccDone = kBarPDSFull + 1;
+  static constexpr int kBarAccDone = kBarPDSFull + 2;
   static constexpr int kBarAccFree = kBarAccDone + 1;
   static constexpr int kBarDrain = kBarAccFree + 1;
   static constexpr int kNumBars = kBarDrain + 1;
@@ -200,6 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[C::kBarSFree], 256);
     mbar_init(&bars[C::kBarDPFull], 1);
     mbar_init(&bars[C::kBarPDSFull], 256);
+    mbar_init(&bars[C::kBarPDSFull + 1], 256);
     mbar_init(&bars[C::kBarAccDone], 1);
     mbar_init(&bars[C::kBarAccFree], 256);
     mbar_init(&bars[C::kBarDrain], 1);
@@ -322,18 +324,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit_w(&bars[C::kBarDPFull]);
         return true;
       };
-      auto issue_acc = [&](uint32_t it, bool acc) {
+      // dV += P^T dO and dK += dS^T Q over the k-steps of P/dS chunk c (queries
+      // 64 w + 32 c .. of both warpgroups w): kk = 2 c, 2 c + 1, 4 + 2 c, 5 + 2 c
+      auto issue_acc = [&](uint32_t it, int c, bool acc) {
         const uint64_t q = dQm + static_cast<uint64_t>(((it % C::kNQ) * C::kTile) >> 4);
         const uint64_t o = dOm + static_cast<uint64_t>(((it % C::kNO) * C::kTile) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
+        for (int i = 0; i < 4; ++i) {
+          const int kk = (i >> 1) * 4 + 2 * c + (i & 1);
           const uint64_t ko = static_cast<uint64_t>((kk * 2048) >> 4);
           const uint32_t pc = tmem + C::kColDP + packed_col(kk);
-          mma_bf16_ts_w(tmem + C::kColDV, pc, o + ko, kIdAcc, (acc || kk > 0) ? 1u : 0u);
-          mma_bf16_ts_w(tmem + C::kColDK, pc + 16u, q + ko, kIdAcc, (acc || kk > 0) ? 1u : 0u);
+          mma_bf16_ts_w(tmem + C::kColDV, pc, o + ko, kIdAcc, (acc || i > 0) ? 1u : 0u);
+          mma_bf16_ts_w(tmem + C::kColDK, pc + 16u, q + ko, kIdAcc, (acc || i > 0) ? 1u : 0u);
         }
-        mma_commit_w(&bars[C::kBarQEmpty + it % C::kNQ]);
-        mma_commit_w(&bars[C::kBarOEmpty + it % C::kNO]);
+        if (c == 1) {
+          mma_commit_w(&bars[C::kBarQEmpty + it % C::kNQ]);
+          mma_commit_w(&bars[C::kBarOEmpty + it % C::kNO]);
+        }
       };
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
         const KvUnit w = make_kv_unit<kPacked, kNoSuffix>(u, sh, vl);
@@ -350,13 +357,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ok = mbar_wait_hint<kHintDkdvMma>(&bars[C::kBarPDSFull], n_pds & 1u, status, vabort);
           if (!ok) break;
-          ++n_pds;
           if (li == 0 && uc > 0) {
             ok = mbar_wait_hint<kHintDkdvMma>(&bars[C::kBarAccFree], (uc - 1) & 1u, status, vabort);
             if (!ok) break;
           }
           tc_fence_after();
-          issue_acc(it, li > 0);
+          issue_acc(it, 0, li > 0);   // runs while the softmax finishes the second chunk
+          ok = mbar_wait_hint<kHintDkdvMma>(&bars[C::kBarPDSFull + 1], n_pds & 1u, status, vabort);
+          if (!ok) break;
+          ++n_pds;
+          tc_fence_after();
+          issue_acc(it, 1, true);
           if (more) ok = issue_dp(it + 1);
         }
         if (!ok) break;
@@ -468,10 +479,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_st16(lane_base + col, pw);
           tmem_st16(lane_base + col + 16, dw);
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&bars[C::kBarPDSFull + ch]);
         }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&bars[C::kBarPDSFull]);
       }
       if (!ok) break;
       qit += w.n;
@@ -551,8 +562,9 @@ struct DqCfg {
   static constexpr int kBarSFull = kBarVEmpty + kNV;
   static constexpr int kBarSFree = kBarSFull + 1;
   static constexpr int kBarDPFull = kBarSFree + 1;
+  // dS written, per 32-column chunk of each warpgroup (chunk c: k-steps with bit 1 = c)
   static constexpr int kBarDSFull = kBarDPFull + 1;
-  static constexpr int kBarDQDone = kBarDSFull + 1;
+  static constexpr int kBarDQDone = kBarDSFull + 2;
   static constexpr int kBarDQFree = kBarDQDone + 1;
   static constexpr int kBarDrain = kBarDQFree + 1;
   static constexpr int kNumBars = kBarDrain + 1;
@@ -655,6 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[C::kBarSFree], 256);
     mbar_init(&bars[C::kBarDPFull], 1);
     mbar_init(&bars[C::kBarDSFull], 256);
+    mbar_init(&bars[C::kBarDSFull + 1], 256);
     mbar_init(&bars[C::kBarDQDone], 1);
     mbar_init(&bars[C::kBarDQFree], 256);
     mbar_init(&bars[C::kBarDrain], 1);
@@ -771,15 +784,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit_w(&bars[C::kBarVEmpty + sv]);   // V is read by dP only
         return true;
       };
-      auto issue_dq = [&](uint32_t it, bool acc) {
+      // dQ += dS K over the k-steps of dS chunk c (keys 64 w + 32 c .. of both warpgroups w):
+      // kk = 2 c, 2 c + 1, 4 + 2 c, 5 + 2 c
+      auto issue_dq = [&](uint32_t it, int c, bool acc) {
         const uint32_t sk = it % C::kNK;
         const uint64_t k = dKm + static_cast<uint64_t>((sk * C::kTile) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
+        for (int i = 0; i < 4; ++i) {
+          const int kk = (i >> 1) * 4 + 2 * c + (i & 1);
           mma_bf16_ts_w(tmem + C::kColDQ, tmem + C::kColDP + packed_col(kk),
-                      k + static_cast<uint64_t>((kk * 2048) >> 4), kIdQ,
-                      (acc || kk > 0) ? 1u : 0u);
-        mma_commit_w(&bars[C::kBarKEmpty + sk]);
+                        k + static_cast<uint64_t>((kk * 2048) >> 4), kIdQ,
+                        (acc || i > 0) ? 1u : 0u);
+        }
+        if (c == 1) mma_commit_w(&bars[C::kBarKEmpty + sk]);
       };
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
         const QUnit w = pick_q_unit<kPacked, kNoSuffix>(u, sh, n_qt, vl);
@@ -796,13 +813,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ok = mbar_wait_hint<kHintDqMma>(&bars[C::kBarDSFull], n_ds & 1u, status, vabort);
           if (!ok) break;
-          ++n_ds;
           if (j == 0 && uc > 0) {
             ok = mbar_wait_hint<kHintDqMma>(&bars[C::kBarDQFree], (uc - 1) & 1u, status, vabort);
             if (!ok) break;
           }
           tc_fence_after();
-          issue_dq(it, j > 0);
+          issue_dq(it, 0, j > 0);   // runs while the softmax finishes the second chunk
+          ok = mbar_wait_hint<kHintDqMma>(&bars[C::kBarDSFull + 1], n_ds & 1u, status, vabort);
+          if (!ok) break;
+          ++n_ds;
+          tc_fence_after();
+          issue_dq(it, 1, true);
           if (more) ok = issue_dp(it + 1);
         }
         if (!ok) break;
@@ -928,10 +949,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             dw[i] = pack_bf16x2(s0, s1);
           }
           tmem_st16(lane_base + col, dw);
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&bars[C::kBarDSFull + ch]);
         }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&bars[C::kBarDSFull]);
       }
       if (!ok) break;
       // epilogue: dQ * s -> bf16; warpgroup 0 stores columns [0, D/2), warpgroup 1 the rest

@@ -51,14 +51,15 @@ struct FwdCfg {
   static constexpr int kOffV = kOffK + kNK * kTile;
   static constexpr int kOffBar = kOffV + kNV * kTile;
   // barriers: q_full, q_empty, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV],
-  //           s_full[2], p_full[2], o_done[2], o_free[2], drain
+  //           s_full[2], p_full[2][2] (per tile, per 64-key half), o_done[2], o_free[2],
+  //           drain
   static constexpr int kBarQFull = 0, kBarQEmpty = 1, kBarKFull = 2;
   static constexpr int kBarKEmpty = kBarKFull + kNK;
   static constexpr int kBarVFull = kBarKEmpty + kNK;
   static constexpr int kBarVEmpty = kBarVFull + kNV;
   static constexpr int kBarSFull = kBarVEmpty + kNV;
   static constexpr int kBarPFull = kBarSFull + 2;
-  static constexpr int kBarODone = kBarPFull + 2;
+  static constexpr int kBarODone = kBarPFull + 4;
   static constexpr int kBarOFree = kBarODone + 2;
   static constexpr int kBarDrain = kBarOFree + 2;
   static constexpr int kNumBars = kBarDrain + 1;
@@ -165,7 +166,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int q = 0; q < 2; ++q) {
       mbar_init(&bars[C::kBarSFull + q], 1);
-      mbar_init(&bars[C::kBarPFull + q], 128);
+      mbar_init(&bars[C::kBarPFull + 2 * q], 128);
+      mbar_init(&bars[C::kBarPFull + 2 * q + 1], 128);
       mbar_init(&bars[C::kBarODone + q], 1);
       mbar_init(&bars[C::kBarOFree + q], 128);
     }
@@ -269,13 +271,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16_ss_w(d, qa + off, ka + off, kIdS, kk > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv = [&](int q, uint32_t vstage, bool acc) {
+      // O_q (+)= P_q V over keys 64 h .. 64 h + 63 (k-steps 4 h .. 4 h + 3)
+      auto issue_pv = [&](int q, uint32_t vstage, int h, bool acc) {
         const uint64_t va = dV0 + static_cast<uint64_t>((vstage * C::kTile) >> 4);
         const uint32_t d = tmem + C::col_o(q), a = tmem + C::col_s(q);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
+        for (int i = 0; i < 4; ++i) {
+          const int kk = 4 * h + i;
           mma_bf16_ts_w(d, a + kk * 8, va + static_cast<uint64_t>((kk * 2048) >> 4), kIdPV,
-                      (acc || kk > 0) ? 1u : 0u);
+                        (acc || i > 0) ? 1u : 0u);
+        }
       };
 
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
@@ -302,16 +307,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool more = (j + 1) < w.n_kt;
           uint32_t ks_next = kit % C::kNK;
           for (int q = 0; q < nq && ok; ++q) {
-            ok = mbar_wait_warp<kHintFwdMma>(&bars[C::kBarPFull + q], (pph >> q) & 1u, status, vabort);
+            ok = mbar_wait_warp<kHintFwdMma>(&bars[C::kBarPFull + 2 * q], (pph >> q) & 1u, status, vabort);
             if (!ok) break;
-            pph ^= 1u << q;
             const uint32_t uqq = q ? uq1 : uq0;
             if (j == 0 && uqq > 0) {
               ok = mbar_wait_warp<kHintFwdMma>(&bars[C::kBarOFree + q], (uqq - 1) & 1u, status, vabort);
               if (!ok) break;
             }
             tc_fence_after();
-            issue_pv(q, vs, j > 0);
+            issue_pv(q, vs, 0, j > 0);   // runs while the softmax finishes the second half
+            ok = mbar_wait_warp<kHintFwdMma>(&bars[C::kBarPFull + 2 * q + 1], (pph >> q) & 1u, status, vabort);
+            if (!ok) break;
+            pph ^= 1u << q;
+            tc_fence_after();
+            issue_pv(q, vs, 1, true);
             if (!more) mma_commit_w(&bars[C::kBarODone + q]);
             if (more) {
               if (q == 0) {
@@ -407,7 +416,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float neg_m = (m_run == -INFINITY) ? 0.0f : -m_run;
         // exponent arguments and the row sum on fp32 pairs (one instruction per two keys);
-        // the sum runs in four independent pair accumulators (16-deep dependent chains)
+        // the sum runs in four independent pair accumulators (16-deep dependent chains).
+        // Each 64-key half of P is signalled as soon as it is in TMEM, unless a row of this
+        // warp raised its running maximum: O is rescaled first then (the P V of this step
+        // accumulates into it), and both halves are signalled after that.
+        const bool any_resc = __any_sync(0xffffffffu, resc);
         const uint64_t c2x2 = f2_pack(c2, c2), nm2 = f2_pack(neg_m, neg_m);
         uint64_t rs2[4] = {f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f),
                            f2_pack(0.0f, 0.0f)};
@@ -427,12 +440,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             pw[i] = pack_bf16x2(p0, p1);
           }
           tmem_st32(lane_base + colS + half * 32, pw);
+          if (!any_resc) {
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&bars[C::kBarPFull + 2 * q + half]);
+          }
         }
         float rs0, rs1, rs2f, rs3;
         f2_unpack(f2_add(rs2[0], rs2[1]), rs0, rs1);
         f2_unpack(f2_add(rs2[2], rs2[3]), rs2f, rs3);
         l += (rs0 + rs1) + (rs2f + rs3);
-        if (__any_sync(0xffffffffu, resc)) {
+        if (any_resc) {
 #pragma unroll
           for (int cc = 0; cc < D / 32; ++cc) {
             uint32_t ov[32];
@@ -442,10 +460,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * factor);
             tmem_st32(lane_base + colO + cc * 32, ov);
           }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&bars[C::kBarPFull + 2 * q]);
+          mbar_arrive(&bars[C::kBarPFull + 2 * q + 1]);
         }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&bars[C::kBarPFull + q]);
       }
       if (!ok) break;
       // epilogue: O / l -> bf16, LSE
