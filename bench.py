@@ -526,6 +526,24 @@ class Group:
         }
 
 
+def replace_slow_groups(groups, rates, alloc, rate, tries=2, frac=0.5):
+    """Reallocate each staging group whose copy rate is below `frac` of the best group's,
+    at most `tries` times per group.  groups / rates are updated in place; alloc(k) returns a
+    new group k, rate(k) measures group k as it now stands.  The replaced groups are returned
+    (the caller keeps them alive, so that the allocator does not hand the same block back)
+    with the number of reallocations."""
+    set_aside, realloc = [], 0
+    for k in range(len(groups)):
+        for _ in range(tries):
+            if rates[k] >= frac * max(rates):
+                break
+            set_aside.append(groups[k])
+            groups[k] = alloc(k)
+            rates[k] = rate(k)
+            realloc += 1
+    return set_aside, realloc
+
+
 class HostResults:
     """Pinned host copies of one step's results, filled on a copy stream while the step
     runs: per response dQ, suffix dK/dV, clip mask and token log-prob (as soon as that
@@ -823,15 +841,9 @@ def run_ours(args, w):
 
         host_groups = [alloc_group(g_) for g_ in dev_groups]
         rates = [copy_gbs(hg, dg) for hg, dg in zip(host_groups, dev_groups)]
-        set_aside, realloc = [], 0
-        for k in range(len(host_groups)):
-            for _ in range(2):
-                if rates[k] >= 0.5 * max(rates):
-                    break
-                set_aside.append(host_groups[k])
-                host_groups[k] = alloc_group(dev_groups[k])
-                rates[k] = copy_gbs(host_groups[k], dev_groups[k])
-                realloc += 1
+        set_aside, realloc = replace_slow_groups(
+            host_groups, rates, lambda k: alloc_group(dev_groups[k]),
+            lambda k: copy_gbs(host_groups[k], dev_groups[k]))
         h2d = sum(t.numel() * t.element_size() for hg in host_groups for t in hg)
         host_loss = torch.empty(1, dtype=torch.float64).pin_memory()
         copy_stream = torch.cuda.Stream()      # host -> device, in consumption order

@@ -62,3 +62,27 @@ def test_warmup_below_three_is_refused(monkeypatch):
     monkeypatch.setattr("sys.argv", ["bench.py", "--warmup", "2"])
     with pytest.raises(SystemExit):
         bench.main()
+
+
+def test_slow_staging_groups_are_replaced_at_most_twice():
+    """The end-to-end harness replaces a pinned staging group that copies below half the best
+    group's rate (kept aside, not freed) and gives up after two tries."""
+    import bench
+    groups = ["g0", "g1", "g2", "g3"]
+    rates = [20.0, 211.0, 210.0, 30.0]
+    # group 0 is fast once reallocated; group 3 stays slow
+    next_rate = {0: [211.0], 3: [40.0, 35.0]}
+    made = []
+
+    def alloc(k):
+        made.append(k)
+        return "g%d'%d" % (k, len([m for m in made if m == k]))
+
+    def rate(k):
+        return next_rate[k].pop(0)
+
+    aside, n = bench.replace_slow_groups(groups, rates, alloc, rate)
+    assert n == 3 and made == [0, 3, 3]
+    assert aside == ["g0", "g3", "g3'1"]
+    assert groups == ["g0'1", "g1", "g2", "g3'2"]
+    assert rates == [211.0, 211.0, 210.0, 35.0]
