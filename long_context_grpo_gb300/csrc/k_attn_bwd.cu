@@ -25,11 +25,13 @@
 // bf16 results: packed P/dS overwrite the fp32 dP columns the softmax has just read, so the
 // S columns are free as soon as S is in registers and the next tile's S = K Q^T (or Q K^T)
 // runs on the tensor pipe while the softmax works; the next dP is issued, in order, after
-// the MMAs that read P/dS.
+// the MMAs that read P/dS.  P/dS are signalled per 32-column chunk of each warpgroup, so the
+// MMAs over the first chunk's k-steps run while the softmax computes the second.
 //
-// Warp roles (384 threads, one CTA per SM): warp 0 TMA producer, warp 1 one MMA-issuing
-// thread, warp 2 TMEM owner, warps 4-11 two softmax warpgroups; warpgroup w owns tile
-// columns [64 w, 64 w + 64).  Every wait is bounded (status word + clean exit on timeout).
+// Warp roles (384 threads, one CTA per SM): warp 0 TMA producer, warp 1 the MMA issuer (a
+// converged warp: every lane polls the waits, one elected lane issues each MMA and commit),
+// warp 2 TMEM owner, warps 4-11 two softmax warpgroups; warpgroup w owns tile columns
+// [64 w, 64 w + 64).  Every wait is bounded (status word + clean exit on timeout).
 //
 // Instantiations <D, kPacked, kNoSuffix> as in the forward: packed responses (a prompt tile
 // then sweeps the Q tiles of every response before its single read-modify-write; Q rows past

@@ -7,8 +7,10 @@
 // GB300 design (one persistent CTA per SM, 384 threads):
 //   warp 0        TMA producer: two Q tiles per work unit, then K and V tiles (128 keys)
 //                 into separate 2-stage rings (prompt keys first, then the causal suffix).
-//   warp 1        one thread issues tcgen05.mma: S_q = Q_q K^T into TMEM (fp32, 128 cols)
-//                 and O_q += P_q V with P_q read back from TMEM (bf16, aliasing S_q).
+//   warp 1        issues tcgen05.mma as a converged warp (one elected lane issues, every
+//                 lane polls the waits): S_q = Q_q K^T into TMEM (fp32, 128 cols) and
+//                 O_q += P_q V with P_q read back from TMEM (bf16, aliasing S_q), each
+//                 64-key half of P_q as soon as the softmax has signalled it.
 //   warp 2        allocates / frees the 512 TMEM columns.
 //   warps 4-7,    softmax warpgroups, one per Q tile; thread = TMEM lane = tile row.
 //   warps 8-11    Online softmax in log2 units with a lazy rescale: the running max only
