@@ -20,6 +20,8 @@ SMALL = {
     "g8_two_tiles": (1000, (300, 129), 16, 2, 128),
     "g16_short": (64, (20, 3), 16, 1, 128),
     "g1_d128_long": (700, (400,), 2, 2, 128),
+    "p1_one_prompt_token": (1, (5, 130), 4, 1, 64),
+    "exact_tiles": (256, (128, 16), 4, 4, 128),
 }
 
 
