@@ -67,3 +67,50 @@ def test_zero_advantage_gives_zero_gradient():
     assert out["loss"] == 0.0
     assert int(out["mask"].sum()) == 0
     assert torch.count_nonzero(out["dlogits"]) == 0
+
+
+def test_loss_single_row():
+    """One token row (the cluster kernel with a single row to walk)."""
+    _check(_run(1, 151936, 0.9))
+
+
+def test_loss_extreme_logits():
+    """Logits with standard deviation 20 (row maxima far above the bulk): the running
+    maximum and the compensated exp sum stay exact to the oracle's tolerances."""
+    _check(_run(256, 32000, -0.6, logit_std=20.0))
+
+
+@pytest.mark.parametrize("V", [151936, 1003], ids=["cluster_kernel", "row_kernel"])
+def test_out_of_range_token_id_sets_status_and_zeroes_its_row(V):
+    """An id outside [0, V) sets the index bit of the device status; that row's loss term,
+    dlogits, clip mask and log-prob are zero, and every other row is the oracle's (the loss
+    still normalised by all R rows)."""
+    import long_context_grpo_gb300 as ls
+    R, A, eps, G = 64, 1.0, 0.2, 4
+    w = wl.Workload("loss", P=1, G=G, Hq=1, Hkv=1, D=64, V=V, R_fixed=(R,), logit_std=2.0,
+                    old_logp_noise=0.1, eps=eps)
+    logits, ids, nz = wl.response_loss_inputs(w, 0, R, 3, "cuda")
+    old = (torch.tensor(oracle.token_logp(logits, ids), dtype=torch.float64) + nz.cpu().double()).float().cuda()
+    ref = oracle.grpo_loss(logits, ids, old, A, eps, G)
+    bad = [5, 40]
+    ids_bad = ids.clone()
+    ids_bad[bad[0]] = -1
+    ids_bad[bad[1]] = V
+    loss = torch.zeros(1, dtype=torch.float64, device="cuda")
+    dlog, mask, logp = ls.grpo_loss(logits, ids_bad, old, A, eps, G, loss)
+    torch.cuda.synchronize()
+    st, bits = ls.device_status()
+    assert bits & 2, (st, bits)
+    good = np.setdiff1d(np.arange(R), bad)
+    surr, _, _ = oracle.surrogate(ref["rho"], A, eps)
+    expect = -(surr[good].sum()) / (G * R)
+    assert abs(float(loss.item()) - expect) <= TOL_LOSS * abs(expect)
+    d = f64(dlog)
+    assert np.all(d[bad] == 0.0)
+    assert rel_l2(dlog[torch.tensor(good, device="cuda")], ref["dlogits"][good]) < TOL_BF16
+    lp = f64(logp)
+    assert np.all(lp[bad] == 0.0)
+    np.testing.assert_allclose(lp[good], ref["logp"][good], atol=2e-5, rtol=0)
+    m = mask.cpu().numpy().astype(bool)
+    assert not m[bad].any()
+    assert ls.device_status() == (0, 0)
