@@ -398,6 +398,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float* rs = rowstats + (static_cast<int64_t>(w.kv) * n_qt + w.f0 + li) * 256;
         const float4* lse4 = reinterpret_cast<const float4*>(rs) + wg * 16;   // rows 64 wg ..
         const float4* dlt4 = reinterpret_cast<const float4*>(rs + 128) + wg * 16;
+        // the next Q tile's row statistics (8 lines of 128 B) into L1 a step ahead, so that
+        // its first reads do not wait on L2
+        if (warp == 4 && lane < 8 && li + 1 < w.n) prefetch_l1(rs + 256 + lane * 32);
         ok = mbar_wait_hint<kHintDkdvSoftmax>(&bars[C::kBarSFull], n_tiles & 1u, status, vabort);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
